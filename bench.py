@@ -1,0 +1,390 @@
+#!/usr/bin/env python3
+"""Benchmark: decode-attention KV-read throughput on one GB300 per rank.
+
+A step is one decode_attn_run (split kernel + LSE merge + range check + recompute pass)
+over the named workload, inputs resident in HBM. Default workload: long-context GQA, batch
+1, 32 query heads over 8 KV heads, head_dim 128, 32768 tokens, bf16 K/V, unified-max
+softmax with the heuristic (balanced) split. The L2 is flushed (256 MiB written) before
+every timed step, outside the timed events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--mode MODE]
+  python bench.py --impl reference ...   # the float64 CPU oracle on the host cores
+
+Under torchrun each rank runs an independent replica of the workload on its own GPU
+(weak scaling); value = all ranks' KV bytes / the slowest rank's time.
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn KV-read GB/s (% of GB300 HBM peak); µs/decode step at 32K GQA"
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="gqa32k")
+    ap.add_argument("--mode", default="unified", choices=["unified", "sync"])
+    ap.add_argument("--num-splits", type=int, default=-1,
+                    help="-1: the plan's heuristic; >0 uniform splits")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "decode_attention_attn_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload_name):
+    """dram read+write bytes per split-kernel launch from the committed ncu summary, or None
+    when the summary is missing or was taken on different kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"split_kernel_{workload_name}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+        return None
+    return int(m_bytes.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        self.proc.wait()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.remove(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def make_attn(binding, _parity, inp, mode, num_splits):
+    plan_splits = 0 if num_splits < 0 else num_splits
+    return binding.DecodeAttention(_parity.problem_for(inp, mode=mode), plan_splits)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import _parity
+    from decode_attention_attn_gb300 import binding, workloads
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev_name = f"cuda:{local}"
+    wl = workloads.get(args.workload)
+    wl = wl.replace(mode=args.mode)
+    inp = workloads.generate(wl, offset=rank)
+    kv_bytes = inp.kv_bytes()
+    dev = _parity.DeviceInputs(inp, dev_name)
+    attn = make_attn(binding, _parity, inp, args.mode, args.num_splits)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev_name)
+    B, H, d = wl.batch, wl.num_q_heads, wl.head_dim
+    out = torch.empty((B, H, d), dtype=workloads.TORCH_DTYPES[wl.out_dtype], device=dev_name)
+    lse = torch.empty((B, H), dtype=torch.float32, device=dev_name)
+    flags = torch.empty((B, H), dtype=torch.uint8, device=dev_name)
+
+    def step(events=None, split_events=None):
+        attn.run(dev.q, dev.k, dev.v, dev.bt, dev.sl, wl.scale, args.num_splits, out=out,
+                 out_lse=lse, row_flags=flags, stream=stream, split_events=split_events)
+
+    # correctness guard on this very launch configuration: sampled rows against the oracle
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    sample_rows = list(range(0, B * H, max(1, (B * H) // 8)))[:8]
+    ref, ref_lse, _, _ = _parity.run_oracle(inp, rows=sample_rows)
+    got = out.reshape(B * H, d)[sample_rows]
+    _parity.compare(got, ref, wl.out_dtype, where="bench guard")
+
+    # ---- timed region: whole steps ----
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    clocks = sampler.stop()
+    if world > 1:
+        dist.barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_local = sum(step_ms) / len(step_ms)
+
+    # ---- split kernel alone (events recorded around its launch), same steps and flushes ----
+    ks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ke = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        step(split_events=(ks[i], ke[i]))
+    torch.cuda.synchronize()
+    kern_ms = sum(s.elapsed_time(e) for s, e in zip(ks, ke)) / args.steps
+
+    ms = ms_local
+    if world > 1:
+        t = torch.tensor([ms_local, kern_ms], device=dev_name)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, kern_ms = float(t[0]), float(t[1])
+
+    # ---- end to end: pinned host inputs -> device -> run -> host results ----
+    e2e = None
+    if not args.no_e2e:
+        hq = inp.q.pin_memory()
+        hk = inp.k_cache.pin_memory()
+        hv = inp.v_cache.pin_memory()
+        hsl = inp.seq_lens.pin_memory()
+        hbt = None if inp.block_table is None else inp.block_table.pin_memory()
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hsl) + ((hbt,) if hbt is not None else ()))
+        d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
+        e_steps = max(5, min(args.steps, 20))
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(e_steps)]
+        ee = [torch.cuda.Event(enable_timing=True) for _ in range(e_steps)]
+        for i in range(e_steps + 2):
+            j = i - 2
+            if j >= 0:
+                es[j].record(stream)
+            dev.q.copy_(hq, non_blocking=True)
+            dev.k.copy_(hk, non_blocking=True)
+            dev.v.copy_(hv, non_blocking=True)
+            dev.sl.copy_(hsl, non_blocking=True)
+            if hbt is not None:
+                dev.bt.copy_(hbt, non_blocking=True)
+            step()
+            hout.copy_(out, non_blocking=True)
+            hlse.copy_(lse, non_blocking=True)
+            if j >= 0:
+                ee[j].record(stream)
+            stream.synchronize()
+        e2e_ms = sum(s.elapsed_time(e) for s, e in zip(es, ee)) / e_steps
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev_name)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t[0])
+        e2e = {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e2e_ms, 4)}
+
+    if world > 1:
+        dist.barrier()
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peak, peak_kind = measured_peaks()
+    achieved = kv_bytes / (kern_ms * 1e-3) / 1e9
+    value = world * kv_bytes / (ms * 1e-3) / 1e9
+    launches_per_step = 2 if args.mode == "unified" else 1
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "us_per_step": round(ms * 1e3, 2),
+        "pct_hbm_peak": round(100 * value / world / peak, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded N(0,1), workloads.py recipe)",
+        "config": {"workload": wl.name, "batch": wl.batch, "q_heads": wl.num_q_heads,
+                   "kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
+                   "kv_tokens_per_seq": int(inp.seq_lens.max()), "kv_dtype": wl.dtype,
+                   "out_dtype": wl.out_dtype, "softmax": args.mode,
+                   "splits": "heuristic (balanced shares)" if args.num_splits < 0 else args.num_splits,
+                   "grid_ctas": attn.info.grid_ctas, "stages": attn.info.stages,
+                   "kv_bytes_per_step": kv_bytes,
+                   "l2": f"flushed ({FLUSH_BYTES >> 20} MiB write) before every timed step",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "kernel": "decode_split_kernel", "kernel_ms": round(kern_ms, 5),
+                     "traffic": profiled_traffic(wl.name)},
+        "clocks": clocks,
+        "gpu_launches": launches_per_step * args.steps,
+        "e2e": e2e,
+        "wall_s_timed": round(t_wall, 3),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def cpu_baseline(inp, seconds):
+    """The float64 CPU oracle, as it stands, on this host's cores over the same inputs."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import _parity
+    import oracle
+    threads = oracle.host_threads()
+    rows = inp.wl.batch * inp.wl.num_q_heads
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        _parity.run_oracle(inp, nthreads=threads)
+        n += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = (time.perf_counter() - t0) / n
+    return {"value": round(inp.kv_bytes() / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle", "ms_per_step": round(dt * 1e3, 2),
+            "sample": f"the whole workload ({rows} query rows, every token), {n} passes"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import _parity
+    import oracle
+    from decode_attention_attn_gb300 import workloads
+    wl = workloads.get(args.workload).replace(mode=args.mode)
+    inp = workloads.generate(wl)
+    threads = oracle.host_threads()
+    for _ in range(args.warmup):
+        _parity.run_oracle(inp, nthreads=threads)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        _parity.run_oracle(inp, nthreads=threads)
+        times.append(time.perf_counter() - t0)
+    dt = sum(times) / len(times)
+    value = inp.kv_bytes() / dt / 1e9
+    rows = wl.batch * wl.num_q_heads
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1), workloads.py recipe)",
+        "config": {"workload": wl.name, "softmax": args.mode,
+                   "kv_bytes_per_step": inp.kv_bytes()},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"the whole workload ({rows} query rows, every token) per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,547 @@
+// da_api.cu -- host side of the C ABI declared in include/decode_attn.h: problem validation,
+// the launch plan (split policy, grid, pipeline depth, workspace layout), TMA tensor maps,
+// kernel launches, error reporting and the debug gather hook.
+#include "decode_attn.h"
+
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <set>
+#include <string>
+#include <utility>
+
+#include "da_device.cuh"
+
+namespace da {
+const void* kernel_f32(int head_dim, int group, bool unified);
+const void* kernel_f16(int head_dim, int group, bool unified);
+const void* kernel_bf16(int head_dim, int group, bool unified);
+
+// The element offset the kernel reads token t of (b, kvh) from: the same token_row() the
+// producer warp uses for its TMA box coordinates.
+__global__ void debug_gather_kernel(const __grid_constant__ Params p) {
+  const long long T = p.capacity;
+  const long long total = (long long)p.batch * p.hkv * T;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(i % T);
+    const int kvh = (int)((i / T) % p.hkv);
+    const int b = (int)(i / T / p.hkv);
+    long long off = -1;
+    const int raw = p.seq_lens[b];
+    const int n = raw < 0 ? 0 : (raw > p.capacity ? p.capacity : raw);
+    if (t < n) {
+      const int entry = p.paged ? p.block_table[(long long)b * p.max_blocks + t / p.page_size] : 0;
+      const int z = token_row(p, b, t, entry);
+      if (z >= 0) off = ((long long)z * p.hkv + kvh) * p.head_dim;
+    }
+    p.debug_offsets[i] = off;
+  }
+}
+}  // namespace da
+
+using namespace da;
+
+struct da_plan {
+  da_problem prob;
+  int num_sms;
+  int group, es, unit, box_tokens, capacity, n_groups;
+  int policy, num_splits;       // the plan's default split choice
+  int grid;                     // balanced grid (or the default uniform grid)
+  int recompute_splits, max_splits;
+  int stages, batch_smem;
+  size_t smem_bytes;
+  long long slots;
+  size_t off_counters, off_list, off_list_state, off_status, off_stats;
+  size_t off_part_flags, off_part_l, off_part_o, zero_bytes, ws_bytes;
+};
+
+namespace {
+
+thread_local std::string g_cuda_error;
+
+int cuda_fail(cudaError_t e, const char* what) {
+  g_cuda_error = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+  return DA_ERR_CUDA;
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+int elem_size(int dt) { return dt == DA_F32 ? 4 : 2; }
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int validate_problem(const da_problem& p) {
+  if (p.batch < 1 || p.num_q_heads < 1 || p.num_kv_heads < 1) return DA_ERR_INVALID_ARG;
+  if (p.num_q_heads % p.num_kv_heads) return DA_ERR_INVALID_ARG;
+  const int G = p.num_q_heads / p.num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return DA_ERR_UNSUPPORTED;
+  if (p.head_dim != 64 && p.head_dim != 128) return DA_ERR_UNSUPPORTED;
+  if (p.qkv_dtype < DA_F32 || p.qkv_dtype > DA_BF16) return DA_ERR_UNSUPPORTED;
+  if (p.out_dtype < DA_F32 || p.out_dtype > DA_BF16) return DA_ERR_UNSUPPORTED;
+  if (p.mode != DA_SOFTMAX_SYNC && p.mode != DA_SOFTMAX_UNIFIED) return DA_ERR_INVALID_ARG;
+  if (p.num_sms < 0) return DA_ERR_INVALID_ARG;
+  if (p.paged) {
+    if (!is_pow2(p.page_size) || p.page_size < 8 || p.page_size > 256) return DA_ERR_UNSUPPORTED;
+    if (p.max_blocks_per_seq < 1 || p.num_physical_blocks < 1) return DA_ERR_INVALID_ARG;
+    if ((long long)p.num_physical_blocks * p.page_size >= (1ll << 31)) return DA_ERR_INVALID_ARG;
+    if ((long long)p.max_blocks_per_seq * p.page_size >= (1ll << 31)) return DA_ERR_INVALID_ARG;
+  } else {
+    if (p.max_seq_len < 1) return DA_ERR_INVALID_ARG;
+    if ((long long)p.batch * p.max_seq_len >= (1ll << 31)) return DA_ERR_INVALID_ARG;
+  }
+  if (p.mode == DA_SOFTMAX_UNIFIED) {
+    if (!std::isfinite(p.unified_max) || !std::isfinite(p.range_lo) ||
+        !std::isfinite(p.range_hi) || !(p.range_lo < p.range_hi))
+      return DA_ERR_INVALID_ARG;
+  }
+  return DA_OK;
+}
+
+const void* kernel_for(const da_plan& pl, bool unified) {
+  switch (pl.prob.qkv_dtype) {
+    case DA_F32: return kernel_f32(pl.prob.head_dim, pl.group, unified);
+    case DA_F16: return kernel_f16(pl.prob.head_dim, pl.group, unified);
+    case DA_BF16: return kernel_bf16(pl.prob.head_dim, pl.group, unified);
+  }
+  return nullptr;
+}
+
+std::mutex g_attr_mu;
+std::set<std::pair<int, const void*>> g_attr_done;
+
+int ensure_smem_attr(const void* fn, size_t smem) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  if (g_attr_done.count({dev, fn})) return DA_OK;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  (void)smem;
+  g_attr_done.insert({dev, fn});
+  return DA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// [tokens, Hkv, D] view of a K or V cache; one box = box_tokens rows of one KV head.
+int make_kv_map(const da_plan& pl, const void* base, CUtensorMap* map) {
+  auto fn = encode_fn();
+  if (!fn) {
+    g_cuda_error = "cuTensorMapEncodeTiled is not available from the driver";
+    return DA_ERR_CUDA;
+  }
+  const da_problem& p = pl.prob;
+  const cuuint64_t tokens = p.paged ? (cuuint64_t)p.num_physical_blocks * p.page_size
+                                    : (cuuint64_t)p.batch * p.max_seq_len;
+  const cuuint64_t dims[3] = {(cuuint64_t)p.head_dim, (cuuint64_t)p.num_kv_heads, tokens};
+  const cuuint64_t strides[2] = {(cuuint64_t)p.head_dim * pl.es,
+                                 (cuuint64_t)p.num_kv_heads * p.head_dim * pl.es};
+  const cuuint32_t box[3] = {(cuuint32_t)p.head_dim, 1u, (cuuint32_t)pl.box_tokens};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUtensorMapDataType dt =
+      pl.es == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  const CUresult r = fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    g_cuda_error = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string((int)r);
+    return DA_ERR_CUDA;
+  }
+  return DA_OK;
+}
+
+void fill_common(const da_plan& pl, Params& k, const int32_t* block_table,
+                 const int32_t* seq_lens, void* ws) {
+  const da_problem& p = pl.prob;
+  std::memset(&k, 0, sizeof k);
+  char* w = static_cast<char*>(ws);
+  k.block_table = block_table;
+  k.seq_lens = seq_lens;
+  if (w) {
+    k.counters = reinterpret_cast<int32_t*>(w + pl.off_counters);
+    k.flag_list = reinterpret_cast<int32_t*>(w + pl.off_list);
+    k.list_state = reinterpret_cast<int32_t*>(w + pl.off_list_state);
+    k.status = reinterpret_cast<int32_t*>(w + pl.off_status);
+    k.stats = reinterpret_cast<unsigned long long*>(w + pl.off_stats);
+    k.part_flags = reinterpret_cast<uint32_t*>(w + pl.off_part_flags);
+    k.part_l = reinterpret_cast<float*>(w + pl.off_part_l);
+    k.part_o = reinterpret_cast<float*>(w + pl.off_part_o);
+  }
+  k.batch = p.batch;
+  k.hq = p.num_q_heads;
+  k.hkv = p.num_kv_heads;
+  k.group = pl.group;
+  k.head_dim = p.head_dim;
+  k.paged = p.paged ? 1 : 0;
+  k.page_size = p.paged ? p.page_size : 1;
+  k.max_blocks = p.paged ? p.max_blocks_per_seq : 0;
+  k.num_blocks = p.paged ? p.num_physical_blocks : 0;
+  k.max_seq_len = p.paged ? 0 : p.max_seq_len;
+  k.capacity = pl.capacity;
+  k.unit = pl.unit;
+  k.box_tokens = pl.box_tokens;
+  k.out_dtype = p.out_dtype;
+  k.n_groups = pl.n_groups;
+  k.stages = pl.stages;
+  k.batch_smem = pl.batch_smem;
+}
+
+int status_to_error(int s) {
+  if (s & kStatusBadBlockTable) return DA_ERR_BAD_BLOCK_TABLE;
+  if (s & kStatusBadSeqLen) return DA_ERR_BAD_SEQ_LEN;
+  if (s & kStatusTimeout) return DA_ERR_DEVICE_TIMEOUT;
+  return DA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int decode_attn_abi_version(void) { return DECODE_ATTN_ABI_VERSION; }
+
+const char* decode_attn_strerror(int code) {
+  switch (code) {
+    case DA_OK: return "success";
+    case DA_ERR_INVALID_ARG: return "invalid argument";
+    case DA_ERR_UNSUPPORTED: return "unsupported head_dim, group size, dtype or page size";
+    case DA_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than the plan requires";
+    case DA_ERR_BAD_BLOCK_TABLE: return "a used block-table entry lies outside the page pool";
+    case DA_ERR_CUDA: return g_cuda_error.empty() ? "CUDA error" : g_cuda_error.c_str();
+    case DA_ERR_DEVICE_TIMEOUT: return "a device pipeline wait ran out of time";
+    case DA_ERR_BAD_SEQ_LEN: return "a sequence length is negative or above the cache capacity";
+    default: return "unknown error code";
+  }
+}
+
+int decode_attn_plan(const da_problem* problem, int num_splits, da_plan** plan_out,
+                     size_t* workspace_bytes_out) {
+  if (!problem || !plan_out || num_splits < 0) return DA_ERR_INVALID_ARG;
+  *plan_out = nullptr;
+  const int v = validate_problem(*problem);
+  if (v != DA_OK) return v;
+  da_plan* pl = new (std::nothrow) da_plan();
+  if (!pl) return DA_ERR_INVALID_ARG;
+  pl->prob = *problem;
+  const da_problem& p = pl->prob;
+  int sms = p.num_sms;
+  if (sms == 0) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) {
+      delete pl;
+      return cuda_fail(e, "querying the SM count");
+    }
+  }
+  pl->num_sms = sms;
+  pl->group = p.num_q_heads / p.num_kv_heads;
+  pl->es = elem_size(p.qkv_dtype);
+  pl->unit = p.paged ? std::max(16, p.page_size) : 16;
+  pl->box_tokens = p.paged ? std::min(p.page_size, kStageTokens) : kStageTokens;
+  pl->capacity = p.paged ? p.max_blocks_per_seq * p.page_size : p.max_seq_len;
+  pl->n_groups = p.batch * p.num_kv_heads;
+  const long long units_max = (pl->capacity + pl->unit - 1) / pl->unit;
+  const long long w_max = (long long)pl->n_groups * units_max;
+  pl->batch_smem = p.batch <= kMaxBatchSmem ? p.batch : 0;
+
+  if (num_splits > 0) {
+    pl->policy = kUniform;
+    pl->num_splits = num_splits;
+  } else if (pl->batch_smem > 0) {
+    // Balanced shares: every persistent CTA gets the same number of KV tokens. A sequence
+    // is split only where a CTA boundary falls inside it, so small batches split finely and
+    // batches that fill the SMs on their own barely split.
+    pl->policy = kBalanced;
+    pl->num_splits = 0;
+  } else {
+    pl->policy = kUniform;
+    pl->num_splits = (int)std::min<long long>(units_max, std::max(1, (sms + pl->n_groups - 1) / pl->n_groups));
+  }
+  const long long min_ctas = (w_max + kMinUnitsPerCta - 1) / kMinUnitsPerCta;
+  pl->grid = pl->policy == kBalanced
+                 ? (int)std::max<long long>(1, std::min<long long>(sms, min_ctas))
+                 : (int)std::min<long long>(sms, (long long)pl->n_groups * pl->num_splits);
+  pl->recompute_splits = (int)std::min<long long>(
+      units_max, std::max(1, (sms + pl->n_groups - 1) / pl->n_groups));
+  const long long need_uniform =
+      (long long)pl->n_groups * std::max(pl->recompute_splits, pl->policy == kUniform ? pl->num_splits : 1);
+  pl->slots = std::max<long long>((long long)sms + pl->n_groups, need_uniform);
+  pl->max_splits = (int)std::min<long long>(1 << 20, pl->slots / pl->n_groups);
+
+  // deepest pipeline that fits the per-CTA shared memory limit
+  pl->stages = 0;
+  for (int s = kMaxStages; s >= 2; --s) {
+    const Layout L = make_layout(p.head_dim, pl->group, pl->es, s, pl->batch_smem);
+    if (L.total <= kSmemLimit) {
+      pl->stages = s;
+      pl->smem_bytes = L.total;
+      break;
+    }
+  }
+  if (pl->stages == 0) {
+    delete pl;
+    return DA_ERR_UNSUPPORTED;
+  }
+
+  const int G = pl->group, D = p.head_dim;
+  size_t off = 0;
+  pl->off_counters = off;
+  off = align256(off + (size_t)pl->n_groups * 4);
+  pl->off_list = off;
+  off = align256(off + (size_t)pl->n_groups * 4);
+  pl->off_list_state = off;
+  pl->off_status = off + 8;
+  pl->off_stats = off + 16;
+  off = align256(off + 32);
+  pl->zero_bytes = off;
+  pl->off_part_flags = off;
+  off = align256(off + (size_t)pl->slots * 4);
+  pl->off_part_l = off;
+  off = align256(off + (size_t)pl->slots * G * 4);
+  pl->off_part_o = off;
+  off = align256(off + (size_t)pl->slots * G * D * 4);
+  pl->ws_bytes = off;
+
+  *plan_out = pl;
+  if (workspace_bytes_out) *workspace_bytes_out = pl->ws_bytes;
+  return DA_OK;
+}
+
+int decode_attn_plan_info(const da_plan* plan, da_plan_info* info) {
+  if (!plan || !info) return DA_ERR_INVALID_ARG;
+  info->grid_ctas = plan->grid;
+  info->num_splits = plan->policy == kBalanced ? 0 : plan->num_splits;
+  info->unit_tokens = plan->unit;
+  info->stage_tokens = kStageTokens;
+  info->stages = plan->stages;
+  info->recompute_splits = plan->recompute_splits;
+  info->max_splits = plan->max_splits;
+  info->workspace_bytes = plan->ws_bytes;
+  info->smem_bytes = plan->smem_bytes;
+  return DA_OK;
+}
+
+void decode_attn_destroy(da_plan* plan) { delete plan; }
+
+int decode_attn_workspace_init(const da_plan* plan, void* workspace, size_t workspace_bytes,
+                               void* cuda_stream) {
+  if (!plan || !workspace || !aligned(workspace, 256)) return DA_ERR_INVALID_ARG;
+  if (workspace_bytes < plan->ws_bytes) return DA_ERR_WORKSPACE_TOO_SMALL;
+  const cudaError_t e =
+      cudaMemsetAsync(workspace, 0, plan->zero_bytes, static_cast<cudaStream_t>(cuda_stream));
+  return e == cudaSuccess ? DA_OK : cuda_fail(e, "cudaMemsetAsync(workspace)");
+}
+
+int decode_attn_run(const da_plan* plan, const void* q, const void* k_cache,
+                    const void* v_cache, const int32_t* block_table, const int32_t* seq_lens,
+                    float scale, int num_splits, void* out, float* out_lse,
+                    uint8_t* row_flags, void* workspace, size_t workspace_bytes,
+                    void* cuda_stream, da_stats* stats) {
+  da_run_args a;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.scale = scale;
+  a.num_splits = num_splits;
+  a.out = out;
+  a.out_lse = out_lse;
+  a.row_flags = row_flags;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.cuda_stream = cuda_stream;
+  a.stats = stats;
+  a.split_event_begin = nullptr;
+  a.split_event_end = nullptr;
+  return decode_attn_run_ex(plan, &a);
+}
+
+int decode_attn_run_ex(const da_plan* plan, const da_run_args* args) {
+  if (!plan || !args) return DA_ERR_INVALID_ARG;
+  const void* q = args->q;
+  const void* k_cache = args->k_cache;
+  const void* v_cache = args->v_cache;
+  const int32_t* block_table = args->block_table;
+  const int32_t* seq_lens = args->seq_lens;
+  const float scale = args->scale;
+  const int num_splits = args->num_splits;
+  void* out = args->out;
+  float* out_lse = args->out_lse;
+  uint8_t* row_flags = args->row_flags;
+  void* workspace = args->workspace;
+  const size_t workspace_bytes = args->workspace_bytes;
+  void* cuda_stream = args->cuda_stream;
+  da_stats* stats = args->stats;
+  if ((args->split_event_begin == nullptr) != (args->split_event_end == nullptr))
+    return DA_ERR_INVALID_ARG;
+  const da_plan& pl = *plan;
+  const da_problem& p = pl.prob;
+  if (!q || !k_cache || !v_cache || !seq_lens || !out || !workspace) return DA_ERR_INVALID_ARG;
+  if (p.paged ? !block_table : block_table != nullptr) return DA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(workspace, 256) || !aligned(seq_lens, 4) || !aligned(out, 16) ||
+      (out_lse && !aligned(out_lse, 4)) || (block_table && !aligned(block_table, 4)))
+    return DA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return DA_ERR_INVALID_ARG;
+  if (num_splits < -1) return DA_ERR_INVALID_ARG;
+  if (workspace_bytes < pl.ws_bytes) return DA_ERR_WORKSPACE_TOO_SMALL;
+  int policy = pl.policy, S = pl.num_splits;
+  if (num_splits == 0) {
+    if (pl.batch_smem == 0) return DA_ERR_UNSUPPORTED;
+    policy = kBalanced;
+    S = 0;
+  } else if (num_splits > 0) {
+    if (num_splits > pl.max_splits) return DA_ERR_WORKSPACE_TOO_SMALL;
+    policy = kUniform;
+    S = num_splits;
+  }
+  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  const bool unified = p.mode == DA_SOFTMAX_UNIFIED;
+
+  CUtensorMap tmk, tmv;
+  int rc = make_kv_map(pl, k_cache, &tmk);
+  if (rc == DA_OK) rc = make_kv_map(pl, v_cache, &tmv);
+  if (rc != DA_OK) return rc;
+
+  Params kp;
+  fill_common(pl, kp, block_table, seq_lens, workspace);
+  kp.q = q;
+  kp.out = out;
+  kp.out_lse = out_lse;
+  kp.row_flags = row_flags;
+  kp.policy = policy;
+  kp.num_splits = S;
+  kp.use_list = 0;
+  kp.write_flags = 1;
+  const double log2e = 1.4426950408889634;
+  kp.qscale = (float)((double)scale * log2e);
+  kp.phi2 = (float)((double)p.unified_max * log2e);
+  kp.lo2 = (float)(((double)p.unified_max + p.range_lo) * log2e);
+  kp.hi2 = (float)(((double)p.unified_max + p.range_hi) * log2e);
+  const int grid = policy == kBalanced
+                       ? pl.grid
+                       : (int)std::min<long long>(pl.num_sms, (long long)pl.n_groups * S);
+
+  const bool sync_after = stats != nullptr || p.validate;
+  char* ws = static_cast<char*>(workspace);
+  cudaError_t e;
+  if (sync_after) {
+    e = cudaMemsetAsync(ws + pl.off_status, 0, 24, stream);   // status + stats counters
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(status)");
+  }
+
+  const void* fn = kernel_for(pl, unified);
+  if (!fn) return DA_ERR_UNSUPPORTED;
+  rc = ensure_smem_attr(fn, pl.smem_bytes);
+  if (rc != DA_OK) return rc;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = pl.smem_bytes;
+  cfg.stream = stream;
+  void* kargs[3] = {&kp, &tmk, &tmv};
+  if (args->split_event_begin) {
+    e = cudaEventRecord(static_cast<cudaEvent_t>(args->split_event_begin), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(split_event_begin)");
+  }
+  e = cudaLaunchKernelExC(&cfg, fn, kargs);
+  if (e != cudaSuccess) return cuda_fail(e, "launching the split kernel");
+  if (args->split_event_end) {
+    e = cudaEventRecord(static_cast<cudaEvent_t>(args->split_event_end), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(split_event_end)");
+  }
+
+  if (unified) {
+    // Synchronised recompute of flagged groups ("The Overflow Fallback: Recomputation").
+    // Always enqueued, as a programmatic dependent of the split kernel, so that no host
+    // round trip is needed; it exits at once when nothing was flagged.
+    Params rp = kp;
+    rp.policy = kUniform;
+    rp.num_splits = pl.recompute_splits;
+    rp.use_list = 1;
+    rp.write_flags = 0;
+    const void* rfn = kernel_for(pl, false);
+    rc = ensure_smem_attr(rfn, pl.smem_bytes);
+    if (rc != DA_OK) return rc;
+    cudaLaunchConfig_t rcfg = cfg;
+    rcfg.gridDim = dim3((unsigned)std::min<long long>(
+        pl.num_sms, (long long)pl.n_groups * pl.recompute_splits));
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    rcfg.attrs = attr;
+    rcfg.numAttrs = 1;
+    void* rargs[3] = {&rp, &tmk, &tmv};
+    e = cudaLaunchKernelExC(&rcfg, rfn, rargs);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the recompute kernel");
+  }
+
+  if (sync_after) {
+    int32_t st = 0;
+    unsigned long long counts[2] = {0, 0};
+    e = cudaMemcpyAsync(&st, ws + pl.off_status, 4, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(counts, ws + pl.off_stats, 16, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device status");
+    if (stats) {
+      stats->grid_ctas = grid;
+      stats->num_splits = policy == kBalanced ? 0 : S;
+      stats->rows_flagged = (long long)counts[0];
+      stats->splits_flagged = (long long)counts[1];
+      stats->recompute_launched = unified ? 1 : 0;
+    }
+    const int err = status_to_error(st);
+    if (err != DA_OK) return err;
+  }
+  return DA_OK;
+}
+
+int decode_attn_check_status(const da_plan* plan, void* workspace, void* cuda_stream) {
+  if (!plan || !workspace) return DA_ERR_INVALID_ARG;
+  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  char* ws = static_cast<char*>(workspace);
+  int32_t st = 0;
+  cudaError_t e = cudaMemcpyAsync(&st, ws + plan->off_status, 4, cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws + plan->off_status, 0, 4, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device status");
+  return status_to_error(st);
+}
+
+int decode_attn_debug_gather(const da_plan* plan, const int32_t* block_table,
+                             const int32_t* seq_lens, int64_t* offsets_out, void* cuda_stream) {
+  if (!plan || !seq_lens || !offsets_out) return DA_ERR_INVALID_ARG;
+  if (plan->prob.paged ? !block_table : block_table != nullptr) return DA_ERR_INVALID_ARG;
+  Params kp;
+  fill_common(*plan, kp, block_table, seq_lens, nullptr);
+  kp.debug_offsets = reinterpret_cast<int64_t*>(offsets_out);
+  debug_gather_kernel<<<std::max(1, std::min(4096, plan->num_sms * 8)), 256, 0,
+                        static_cast<cudaStream_t>(cuda_stream)>>>(kp);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? DA_OK : cuda_fail(e, "launching the debug gather kernel");
+}
+
+}  // extern "C"

@@ -1,0 +1,295 @@
+// da_device.cuh -- launch parameters, shared-memory layout and sm_103a PTX helpers of the
+// decode-attention kernels (TMA tensor loads, bulk copies, mbarriers, programmatic
+// dependent launch, exp2 / log2, packed FP32 FMA).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace da {
+
+// ---- fixed kernel geometry ------------------------------------------------------------
+constexpr int kConsumerWarps = 8;                       // compute warps per CTA
+constexpr int kThreads = (kConsumerWarps + 1) * 32;     // + one TMA producer warp
+constexpr int kTokensPerWarp = 8;                       // KV rows a consumer warp takes per stage
+constexpr int kStageTokens = kConsumerWarps * kTokensPerWarp;   // 64 KV rows per stage
+constexpr int kMaxStages = 8;
+constexpr int kMaxBatchSmem = 2048;                     // balanced schedule keeps B lengths in smem
+constexpr uint32_t kSmemLimit = 232448;                 // 227 KB opt-in per CTA
+constexpr int kMinUnitsPerCta = 8;                      // no share below 8 units (128 tokens)
+
+// status bits recorded by the device in the workspace
+constexpr int kStatusBadBlockTable = 1;
+constexpr int kStatusBadSeqLen = 2;
+constexpr int kStatusTimeout = 4;
+
+// bound on any pipeline wait (ns); a healthy wait lasts microseconds
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+enum Policy { kBalanced = 0, kUniform = 1 };
+enum OutType { kOutF32 = 0, kOutF16 = 1, kOutBF16 = 2 };
+
+struct Params {
+  const void* q;                 // [B, Hq, D]
+  const int32_t* block_table;    // [B, max_blocks] (paged)
+  const int32_t* seq_lens;       // [B]
+  void* out;                     // [B, Hq, D] out dtype
+  float* out_lse;                // [B, Hq] or null
+  uint8_t* row_flags;            // [B, Hq] or null
+  int32_t* counters;             // [n_groups] arrivals per group (self-cleaning)
+  int32_t* flag_list;            // [n_groups] flagged groups (unified main pass)
+  int32_t* list_state;           // [0] flagged count, [1] recompute CTAs finished
+  int32_t* status;               // device findings
+  unsigned long long* stats;     // [0] rows flagged, [1] split partials flagged
+  uint32_t* part_flags;          // [slots] range-check bits per head
+  float* part_l;                 // [slots, G] log2-domain LSE of each partial
+  float* part_o;                 // [slots, G, D] normalised partial outputs
+  int64_t* debug_offsets;        // debug gather output
+  int batch, hq, hkv, group, head_dim;
+  int paged, page_size, max_blocks, num_blocks, max_seq_len;
+  int capacity;                  // token capacity of one sequence
+  int unit;                      // split boundaries fall on multiples of this many tokens
+  int box_tokens;                // KV rows per TMA box
+  int out_dtype;
+  int policy;                    // kBalanced / kUniform
+  int num_splits;                // uniform: splits per group
+  int use_list;                  // recompute pass: groups come from flag_list
+  int write_flags;               // main unified pass: flags, flagged list, stats
+  int n_groups;                  // B * Hkv
+  int stages;                    // pipeline depth
+  int batch_smem;                // lengths held in smem (balanced) or 0
+  float qscale;                  // scale * log2(e): logits come out in log2 units
+  float phi2, lo2, hi2;          // unified constant and range bounds, log2 units
+};
+
+// ---- shared-memory layout (host and device compute it identically) ------------------------
+struct Layout {
+  uint32_t stage_bytes, k_off, v_off, q_off;
+  uint32_t bar_off, pbuf_off, mm_off, ml_off, mflag_off, macc_off, lens_off, prefix_off, misc_off;
+  uint32_t total;
+};
+
+__host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline Layout make_layout(int D, int G, int es, int stages, int batch_smem) {
+  Layout L;
+  const uint32_t kv = (uint32_t)kStageTokens * D * es;
+  L.k_off = 0;
+  L.v_off = kv;
+  L.q_off = 2 * kv;
+  L.stage_bytes = align_up(2 * kv + (uint32_t)G * D * es, 128);
+  uint32_t off = (uint32_t)stages * L.stage_bytes;
+  L.bar_off = off;
+  off += 2u * stages * 8u;
+  off = align_up(off, 16);
+  L.pbuf_off = off;
+  off += (uint32_t)kConsumerWarps * kTokensPerWarp * G * 4u;
+  L.mm_off = off;
+  off += (uint32_t)kConsumerWarps * G * 4u;
+  L.ml_off = off;
+  off += (uint32_t)kConsumerWarps * G * 4u;
+  L.mflag_off = off;
+  off += (uint32_t)kConsumerWarps * 4u;
+  off = align_up(off, 16);
+  L.macc_off = off;
+  off += (uint32_t)kConsumerWarps * G * D * 4u;
+  L.lens_off = off;
+  off += (uint32_t)batch_smem * 4u;
+  L.prefix_off = off;
+  off += (uint32_t)(batch_smem + 1) * 4u;
+  off = align_up(off, 16);
+  L.misc_off = off;
+  off += 16;
+  L.total = off + 128;   // slack for aligning the dynamic smem base to 128 bytes
+  return L;
+}
+
+#ifdef __CUDACC__
+// ---- PTX helpers ---------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase of `parity` to complete, for at most kWaitLimitNs. Returns false on
+// timeout (the caller records it and degrades to a non-waiting completion).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+__device__ __forceinline__ uint64_t make_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// 3-D tiled TMA load of a box into shared memory, completing on `bar` by transaction bytes.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y, int z, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)),
+      "l"(policy)
+      : "memory");
+}
+
+// Contiguous bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float fast_log2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Two FP32 fused multiply-adds in one instruction: (d.x, d.y) = (a.x * b.x + d.x, a.y * b.y + d.y)
+__device__ __forceinline__ void ffma2(float2& d, const float2 a, const float2 b) {
+  unsigned long long dd, aa, bb;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(aa) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(bb) : "f"(b.x), "f"(b.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(dd) : "f"(d.x), "f"(d.y));
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(dd) : "l"(aa), "l"(bb));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(dd));
+}
+
+// ---- element conversion of one 16-byte chunk to FP32 ------------------------------------
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<float> {
+  static constexpr int kPerChunk = 4;
+  __device__ __forceinline__ static void to_f32(const uint4 c, float* f) {
+    f[0] = __uint_as_float(c.x);
+    f[1] = __uint_as_float(c.y);
+    f[2] = __uint_as_float(c.z);
+    f[3] = __uint_as_float(c.w);
+  }
+};
+
+template <>
+struct Elem<__nv_bfloat16> {
+  static constexpr int kPerChunk = 8;
+  // bfloat16 is the upper half of a binary32: widening is a shift / mask.
+  __device__ __forceinline__ static void to_f32(const uint4 c, float* f) {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+};
+
+template <>
+struct Elem<__half> {
+  static constexpr int kPerChunk = 8;
+  __device__ __forceinline__ static void to_f32(const uint4 c, float* f) {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __half2 h;
+      memcpy(&h, &w[i], 4);
+      const float2 v = __half22float2(h);
+      f[2 * i] = v.x;
+      f[2 * i + 1] = v.y;
+    }
+  }
+};
+
+__device__ __forceinline__ void store_out(void* out, int64_t idx, int type, float v) {
+  if (type == kOutF32)
+    static_cast<float*>(out)[idx] = v;
+  else if (type == kOutF16)
+    static_cast<__half*>(out)[idx] = __float2half_rn(v);
+  else
+    static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+}
+
+// Token t of sequence b -> row coordinate z of the [tokens, Hkv, D] view of the cache
+// ("FlashAttention and inference kernels", "PagedAttention": slot t % page of physical
+// block block_table[t / page]). `entry` is the block-table entry for t's page (paged).
+// Returns -1 for an entry outside the pool.
+__device__ __forceinline__ int token_row(const Params& p, int b, int t, int entry) {
+  if (p.paged) {
+    if (entry < 0 || entry >= p.num_blocks) return -1;
+    return entry * p.page_size + (t & (p.page_size - 1));
+  }
+  return b * p.max_seq_len + t;
+}
+#endif  // __CUDACC__
+
+}  // namespace da

@@ -1,0 +1,693 @@
+// da_kernel.cuh -- the split-KV decode-attention kernel for sm_103a.
+//
+// One persistent CTA per SM walks a list of "pieces": (sequence b, KV head kvh, token
+// range [t0, t1)). A piece is one Flash-Decoding split ("Flash-Decoding: Mathematical
+// Foundations, ...", "Mathematical Formulation of Split-KV Parallelism"): it yields the
+// partial output O, the maximum m and the sum l for all G query heads of its KV head at
+// once, so each KV row is read from HBM once for the whole group ("FlashAttention and
+// inference kernels", Exercise 3).
+//
+// Warp roles:
+//   warp 8      producer: TMA-loads 64-row K and V tiles (and, per piece, the group's q)
+//               into a ring of shared-memory stages; paged caches are gathered through the
+//               block table one page per TMA box ("PagedAttention").
+//   warps 0..7  consumers: each takes 8 rows of every stage. A row of d elements is split
+//               over a lane group (16 lanes for d = 128 in 16-bit types, 16-byte chunks per
+//               lane); q . k partial sums for all heads and rows of the lane group are
+//               completed by a butterfly transpose-reduce that leaves one (row, head) logit
+//               per lane, so every lane does one exponential. Softmax:
+//                 SYNC    -- online softmax with the running maximum per head, rescaling
+//                            the accumulators by exp(m_old - m_new) ("FlashAttention:
+//                            tiling plus online softmax");
+//                 UNIFIED -- exp(x - phi) against the one constant phi, no maximum, no
+//                            rescaling, and a range check of x - phi against the closed
+//                            interval [lo, hi] (FlashDecoding++, Eq. 3, Eq. 4, Fig. 6).
+//               P . V then accumulates into per-lane FP32 registers.
+// At a piece's end the 8 consumer warps' states are combined in shared memory into one
+// partial (normalised O, L = m + log l). A group covered by a single piece is written out
+// directly; otherwise the partial goes to the workspace and the CTA that completes the
+// group's last piece (an atomic arrival counter, no waiting) performs the exact log-sum-exp
+// merge ("The Rescaling and Online Softmax Reduction Algorithm").
+//
+// All exponentials are base 2: q is pre-multiplied by scale * log2(e), and log-sum-exps
+// are converted back to natural log on output.
+#pragma once
+
+#include "da_device.cuh"
+
+namespace da {
+
+template <typename T, int D, int G>
+struct Cfg {
+  static constexpr int kEs = sizeof(T);
+  static constexpr int kEpl = 16 / kEs;               // elements per 16-byte chunk
+  static constexpr int kLg = D / kEpl;                // lanes per KV row (lane group)
+  static constexpr int kNlg = 32 / kLg;               // lane groups per warp
+  static constexpr int kT = kTokensPerWarp / kNlg;    // rows per lane group per stage
+  static constexpr int kV = G * kT;                   // logits per lane group per stage
+  static constexpr int kNv = kV >= kLg ? kV / kLg : 1;    // complete logits per lane
+  static constexpr int kRep = kV >= kLg ? 1 : kLg / kV;   // lanes that hold the same logit
+  static constexpr int kRowBytes = D * kEs;
+  static constexpr int kQBytes = G * D * kEs;
+  static_assert(kLg >= 1 && kLg <= 32 && (32 % kLg) == 0, "a row must span a lane group");
+  static_assert((kTokensPerWarp % kNlg) == 0, "rows per warp must split over lane groups");
+  static_assert((kV & (kV - 1)) == 0, "logit count must be a power of two");
+  static_assert((kQBytes % 16) == 0, "q bulk copy must be a multiple of 16 bytes");
+};
+
+// Butterfly transpose-reduce over the O*2 lanes of a lane group. Each lane starts with N
+// partial sums (index = row * G + head); at every step a lane keeps half of its values
+// (the upper half if its lane bit O is set), sends the other half to its partner and adds
+// what it receives. After log2(N) halvings each lane holds complete sums of consecutive
+// indices; further steps are plain butterfly adds (lanes then hold replicated values).
+template <int N, int O>
+struct Reduce {
+  __device__ __forceinline__ static void run(float* v, int lane) {
+    if constexpr (O == 0) {
+      return;
+    } else if constexpr (N > 1) {
+      constexpr int H = N / 2;
+      const bool upper = (lane & O) != 0;
+#pragma unroll
+      for (int i = 0; i < H; ++i) {
+        const float a = v[i], b = v[i + H];
+        const float send = upper ? a : b;
+        const float keep = upper ? b : a;
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+      }
+      Reduce<H, O / 2>::run(v, lane);
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
+      Reduce<1, O / 2>::run(v, lane);
+    }
+  }
+};
+
+struct Piece {
+  int g, b, kvh;
+  int t0, t1;        // token range of this piece
+  int nslots;        // pieces of the group (1: write the output directly)
+  int slot_base;     // partial index of the group's first piece
+  int slot;          // this piece's partial index
+};
+
+struct Sched {
+  int policy;
+  long long u, u1, W;    // balanced: unit cursor, end, total units
+  int P, c;
+  long long i, i1;       // uniform: item cursor, end
+  int S;
+  const int* lens;       // balanced: clamped lengths (smem)
+  const int* prefix;     // balanced: exclusive prefix of units per sequence (smem)
+};
+
+__device__ __forceinline__ int clamp_len(const Params& p, int n) {
+  return n < 0 ? 0 : (n > p.capacity ? p.capacity : n);
+}
+
+// CTA whose balanced share [floor(c W / P), floor((c + 1) W / P)) holds unit u.
+__device__ __forceinline__ long long cta_of(long long u, long long W, int P) {
+  return ((u + 1) * P - 1) / W;
+}
+
+__device__ __forceinline__ bool sched_next(Sched& s, const Params& p, Piece& pc) {
+  if (s.policy == kBalanced) {
+    if (s.u >= s.u1) return false;
+    const long long u = s.u;
+    const long long hkv = p.hkv;
+    int lo = 0, hi = p.batch;   // invariant: hkv * prefix[lo] <= u < hkv * prefix[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (hkv * s.prefix[mid] <= u) lo = mid; else hi = mid;
+    }
+    const int b = lo;
+    const long long nb = s.prefix[b + 1] - s.prefix[b];
+    const long long base = hkv * s.prefix[b];
+    const int kvh = (int)((u - base) / nb);
+    const long long gs = base + kvh * nb, ge = gs + nb;
+    const long long pe = s.u1 < ge ? s.u1 : ge;
+    const long long n = s.lens[b];
+    pc.b = b;
+    pc.kvh = kvh;
+    pc.g = b * p.hkv + kvh;
+    pc.t0 = (int)((u - gs) * p.unit);
+    const long long t1 = (pe - gs) * p.unit;
+    pc.t1 = (int)(t1 < n ? t1 : n);
+    const long long cf = cta_of(gs, s.W, s.P), cl = cta_of(ge - 1, s.W, s.P);
+    pc.nslots = (int)(cl - cf + 1);
+    pc.slot_base = (int)cf + pc.g;
+    pc.slot = s.c + pc.g;
+    s.u = pe;
+    return true;
+  }
+  if (s.i >= s.i1) return false;
+  const long long i = s.i++;
+  const int li = (int)(i / s.S), sp = (int)(i % s.S);
+  const int g = p.use_list ? __ldcg(p.flag_list + li) : li;
+  const int b = g / p.hkv;
+  const int n = clamp_len(p, __ldg(p.seq_lens + b));
+  const int ts = n == 0 ? 0 : ((n + s.S - 1) / s.S + p.unit - 1) / p.unit * p.unit;
+  const long long t0 = (long long)sp * ts < n ? (long long)sp * ts : n;
+  const long long t1 = t0 + ts < n ? t0 + ts : n;
+  pc.g = g;
+  pc.b = b;
+  pc.kvh = g - b * p.hkv;
+  pc.t0 = (int)t0;
+  pc.t1 = (int)t1;
+  pc.nslots = s.S;
+  pc.slot_base = g * s.S;
+  pc.slot = g * s.S + sp;
+  return true;
+}
+
+// ---- producer warp -------------------------------------------------------------------
+template <typename T, int D, int G>
+__device__ __forceinline__ void run_producer(const Params& p, Sched s, uint8_t* stages,
+                                             const Layout& L, uint64_t* full, uint64_t* empty,
+                                             const CUtensorMap* tmk, const CUtensorMap* tmv,
+                                             int lane) {
+  using C = Cfg<T, D, G>;
+  const uint64_t pol = make_evict_first_policy();
+  const uint32_t NS = (uint32_t)p.stages;
+  uint32_t k = 0;
+  bool dead = false;
+  Piece pc;
+  while (sched_next(s, p, pc)) {
+    if (pc.t1 <= pc.t0) continue;
+    const int32_t* trow = p.paged ? p.block_table + (long long)pc.b * p.max_blocks : nullptr;
+    const char* qsrc = static_cast<const char*>(p.q) +
+                       ((long long)pc.b * p.hq + (long long)pc.kvh * G) * D * C::kEs;
+    int wbase = -1, nbase = -1;
+    int32_t win = -1, wnext = -1;
+    for (int ts = pc.t0, j = 0; ts < pc.t1; ts += kStageTokens, ++j, ++k) {
+      const uint32_t slot = k % NS, ph = (k / NS) & 1u;
+      if (!dead && !mbar_wait(&empty[slot], ph ^ 1u)) {
+        dead = true;
+        if (lane == 0) atomicOr(p.status, kStatusTimeout);
+      }
+      const int n = min(kStageTokens, pc.t1 - ts);
+      uint8_t* st = stages + slot * L.stage_bytes;
+      if (p.paged) {
+        const int box = p.box_tokens;
+        const int nbox = (n + box - 1) / box;
+        int zs[kStageTokens / 8];
+#pragma unroll
+        for (int bi = 0; bi < kStageTokens / 8; ++bi) {
+          if (bi < nbox) {   // warp-uniform
+            const int t = ts + bi * box;
+            const int page = t / p.page_size;
+            const int base = page & ~31;
+            if (base != wbase) {
+              if (base == nbase) {
+                win = wnext;
+              } else {
+                const int idx = base + lane;
+                win = idx < p.max_blocks ? __ldg(trow + idx) : -1;
+              }
+              wbase = base;
+              nbase = base + 32;
+              const int nidx = nbase + lane;
+              wnext = nidx < p.max_blocks ? __ldg(trow + nidx) : -1;   // prefetch next window
+            }
+            const int entry = __shfl_sync(0xffffffffu, win, page & 31);
+            int z = token_row(p, pc.b, t, entry);
+            if (z < 0) {
+              if (lane == 0) atomicOr(p.status, kStatusBadBlockTable);
+              z = p.num_blocks * p.page_size;   // past the pool: the box reads as zeros
+            }
+            zs[bi] = z;
+          }
+        }
+        if (lane == 0 && !dead) {
+          const uint32_t bytes =
+              (uint32_t)nbox * box * C::kRowBytes * 2u + (j == 0 ? (uint32_t)C::kQBytes : 0u);
+          mbar_arrive_expect_tx(&full[slot], bytes);
+          if (j == 0) bulk_load(st + L.q_off, qsrc, C::kQBytes, &full[slot]);
+#pragma unroll
+          for (int bi = 0; bi < kStageTokens / 8; ++bi) {
+            if (bi < nbox) {
+              tma_load_3d(st + L.k_off + bi * box * C::kRowBytes, tmk, &full[slot], 0, pc.kvh,
+                          zs[bi], pol);
+              tma_load_3d(st + L.v_off + bi * box * C::kRowBytes, tmv, &full[slot], 0, pc.kvh,
+                          zs[bi], pol);
+            }
+          }
+        }
+      } else if (lane == 0 && !dead) {
+        const uint32_t bytes =
+            (uint32_t)kStageTokens * C::kRowBytes * 2u + (j == 0 ? (uint32_t)C::kQBytes : 0u);
+        const int z = pc.b * p.max_seq_len + ts;
+        mbar_arrive_expect_tx(&full[slot], bytes);
+        if (j == 0) bulk_load(st + L.q_off, qsrc, C::kQBytes, &full[slot]);
+        tma_load_3d(st + L.k_off, tmk, &full[slot], 0, pc.kvh, z, pol);
+        tma_load_3d(st + L.v_off, tmv, &full[slot], 0, pc.kvh, z, pol);
+      }
+      __syncwarp();
+    }
+  }
+  // Never leave with copies in flight: wait (bounded) for the last issued stages to land.
+  if (!dead && lane == 0) {
+    const uint32_t first = k > NS ? k - NS : 0u;
+    for (uint32_t kk = first; kk < k; ++kk) mbar_wait(&full[kk % NS], (kk / NS) & 1u);
+  }
+}
+
+// ---- consumer warps: one stage ----------------------------------------------------------
+template <typename T, int D, int G, bool UNIFIED>
+__device__ __forceinline__ void consume_stage(const Params& p, const uint8_t* ks,
+                                              const uint8_t* vs, int n, int warp, int lane,
+                                              const float (&q)[G][Cfg<T, D, G>::kEpl],
+                                              float (&acc)[G][Cfg<T, D, G>::kEpl],
+                                              float (&den)[G], float (&m)[G], uint32_t& fmask,
+                                              float* pwarp) {
+  using C = Cfg<T, D, G>;
+  constexpr int E = C::kEpl;
+  const int lg = lane / C::kLg, li = lane % C::kLg;
+  const int row0 = warp * kTokensPerWarp + lg * C::kT;
+  float* pw = pwarp + lg * C::kV;
+
+  // q . k for the lane group's rows and all G heads: partial sums over this lane's chunk
+  float part[C::kV];
+#pragma unroll
+  for (int j = 0; j < C::kT; ++j) {
+    const uint4 c = *reinterpret_cast<const uint4*>(ks + (row0 + j) * C::kRowBytes + li * 16);
+    float kf[E];
+    Elem<T>::to_f32(c, kf);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int e = 0; e < E; e += 2)
+        ffma2(s2, make_float2(q[g][e], q[g][e + 1]), make_float2(kf[e], kf[e + 1]));
+      part[j * G + g] = s2.x + s2.y;
+    }
+  }
+  Reduce<C::kV, C::kLg / 2>::run(part, lane);
+
+  // this lane's complete logits: index = row * G + head
+  int gi[C::kNv];
+  bool valid[C::kNv];
+#pragma unroll
+  for (int i = 0; i < C::kNv; ++i) {
+    const int idx = C::kV >= C::kLg ? li * C::kNv + i : li / C::kRep;
+    gi[i] = idx % G;
+    valid[i] = row0 + idx / G < n;
+  }
+  const bool writer = (li % C::kRep) == 0;
+
+  if constexpr (UNIFIED) {
+#pragma unroll
+    for (int i = 0; i < C::kNv; ++i) {
+      const float s = part[i];
+      const float pr = valid[i] ? fast_exp2(s - p.phi2) : 0.f;
+      if (valid[i] && (s < p.lo2 || s > p.hi2)) fmask |= 1u << gi[i];
+      const int idx = C::kV >= C::kLg ? li * C::kNv + i : li / C::kRep;
+      if (writer) pw[idx] = pr;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < C::kNv; ++i) {
+      const int idx = C::kV >= C::kLg ? li * C::kNv + i : li / C::kRep;
+      if (writer) pw[idx] = valid[i] ? part[i] : -INFINITY;
+    }
+    __syncwarp();
+    // per-head maximum over the warp's 8 rows of this stage, then the online update
+    float tm[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) tm[g] = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < kTokensPerWarp; ++r)
+#pragma unroll
+      for (int g = 0; g < G; ++g) tm[g] = fmaxf(tm[g], pwarp[r * G + g]);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float mn = fmaxf(m[g], tm[g]);
+      const float alpha = mn == -INFINITY ? 1.f : fast_exp2(m[g] - mn);
+      m[g] = mn;
+      den[g] *= alpha;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[g][e] *= alpha;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < C::kNv; ++i) {
+      float mg = m[0];
+#pragma unroll
+      for (int g = 1; g < G; ++g)
+        if (gi[i] == g) mg = m[g];
+      const float pr = valid[i] ? fast_exp2(part[i] - mg) : 0.f;
+      const int idx = C::kV >= C::kLg ? li * C::kNv + i : li / C::kRep;
+      if (writer) pw[idx] = pr;
+    }
+  }
+  __syncwarp();
+
+  // P . V: every lane of the group accumulates its chunk of d for all heads
+#pragma unroll
+  for (int j = 0; j < C::kT; ++j) {
+    if (row0 + j < n) {
+      const uint4 c = *reinterpret_cast<const uint4*>(vs + (row0 + j) * C::kRowBytes + li * 16);
+      float vf[E];
+      Elem<T>::to_f32(c, vf);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float pr = pw[j * G + g];
+        den[g] += pr;
+        const float2 pp = make_float2(pr, pr);
+#pragma unroll
+        for (int e = 0; e < E; e += 2) {
+          float2 a2 = make_float2(acc[g][e], acc[g][e + 1]);
+          ffma2(a2, pp, make_float2(vf[e], vf[e + 1]));
+          acc[g][e] = a2.x;
+          acc[g][e + 1] = a2.y;
+        }
+      }
+    }
+  }
+  __syncwarp();
+}
+
+// ---- consumer warps: end of a piece ---------------------------------------------------
+template <typename T, int D, int G, bool UNIFIED>
+__device__ __forceinline__ void finish_piece(const Params& p, const Piece& pc,
+                                             float (&acc)[G][Cfg<T, D, G>::kEpl],
+                                             float (&den)[G], const float (&m)[G],
+                                             uint32_t fmask, float* mm, float* ml,
+                                             uint32_t* mflag, float* macc, int* misc, int warp,
+                                             int lane, int ctid) {
+  using C = Cfg<T, D, G>;
+  constexpr int E = C::kEpl;
+  constexpr int kCT = kConsumerWarps * 32;
+  constexpr float kLn2 = 0.6931471805599453f;
+  const int lg = lane / C::kLg, li = lane % C::kLg;
+
+  // combine the warp's lane groups (same d-chunk, disjoint rows)
+#pragma unroll
+  for (int o = C::kLg; o < 32; o <<= 1) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      den[g] += __shfl_xor_sync(0xffffffffu, den[g], o);
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], o);
+    }
+  }
+  const uint32_t fm = __reduce_or_sync(0xffffffffu, fmask);
+  if (lg == 0) {
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int e = 0; e < E; ++e) macc[(warp * G + g) * D + li * E + e] = acc[g][e];
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      mm[warp * G + g] = m[g];
+      ml[warp * G + g] = den[g];
+    }
+    mflag[warp] = fm;
+  }
+  named_bar_sync(1, kCT);
+
+  uint32_t fl = 0;
+#pragma unroll
+  for (int w = 0; w < kConsumerWarps; ++w) fl |= mflag[w];
+  const bool direct = pc.nslots == 1;
+  const long long row0 = (long long)pc.b * p.hq + (long long)pc.kvh * G;
+
+  // the 8 warps' (m, l, acc) -> one partial: max-rescale merge within the CTA
+  for (int e = ctid; e < G * D; e += kCT) {
+    const int g = e / D, d = e - (e / D) * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w)
+      if (ml[w * G + g] > 0.f) M = fmaxf(M, mm[w * G + g]);
+    float num = 0.f, sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float l = ml[w * G + g];
+      if (l > 0.f) {
+        const float f = fast_exp2(mm[w * G + g] - M);
+        sum += f * l;
+        num += f * macc[(w * G + g) * D + d];
+      }
+    }
+    const float o = sum > 0.f ? num / sum : 0.f;
+    const float L2 = sum > 0.f ? M + fast_log2(sum) : -INFINITY;
+    if (direct) {
+      store_out(p.out, (row0 + g) * D + d, p.out_dtype, o);
+      if (d == 0) {
+        if (p.out_lse) p.out_lse[row0 + g] = L2 * kLn2;
+        if (p.row_flags && p.write_flags) p.row_flags[row0 + g] = (uint8_t)((fl >> g) & 1u);
+      }
+    } else {
+      __stcg(p.part_o + ((long long)pc.slot * G + g) * D + d, o);
+      if (d == 0) __stcg(p.part_l + (long long)pc.slot * G + g, L2);
+    }
+  }
+  if (ctid == 0 && p.write_flags && fl) {
+    atomicAdd(p.stats + 1, (unsigned long long)__popc(fl));
+    if (direct) {
+      atomicAdd(p.stats + 0, (unsigned long long)__popc(fl));
+      const int at = atomicAdd(p.list_state, 1);
+      if (at < p.n_groups) p.flag_list[at] = pc.g;
+    }
+  }
+
+  if (!direct) {
+    if (ctid == 0) __stcg(p.part_flags + pc.slot, fl);
+    __threadfence();
+    named_bar_sync(1, kCT);
+    if (ctid == 0) {
+      const int old = atomicAdd(p.counters + pc.g, 1);
+      misc[0] = old == pc.nslots - 1;
+    }
+    named_bar_sync(1, kCT);
+    if (misc[0]) {
+      // last piece of the group: exact log-sum-exp merge of all its partials
+      __threadfence();
+      uint32_t rf = 0;
+      for (int s = 0; s < pc.nslots; ++s) rf |= __ldcg(p.part_flags + pc.slot_base + s);
+      for (int e = ctid; e < G * D; e += kCT) {
+        const int g = e / D, d = e - (e / D) * D;
+        float Lm = -INFINITY;
+        for (int s = 0; s < pc.nslots; ++s)
+          Lm = fmaxf(Lm, __ldcg(p.part_l + (long long)(pc.slot_base + s) * G + g));
+        float num = 0.f, sum = 0.f;
+        if (Lm > -INFINITY) {
+          for (int s = 0; s < pc.nslots; ++s) {
+            const float Ls = __ldcg(p.part_l + (long long)(pc.slot_base + s) * G + g);
+            if (Ls > -INFINITY) {
+              const float f = fast_exp2(Ls - Lm);
+              sum += f;
+              num += f * __ldcg(p.part_o + ((long long)(pc.slot_base + s) * G + g) * D + d);
+            }
+          }
+        }
+        const float o = sum > 0.f ? num / sum : 0.f;
+        store_out(p.out, (row0 + g) * D + d, p.out_dtype, o);
+        if (d == 0) {
+          if (p.out_lse) p.out_lse[row0 + g] = sum > 0.f ? (Lm + fast_log2(sum)) * kLn2 : -INFINITY;
+          if (p.row_flags && p.write_flags) p.row_flags[row0 + g] = (uint8_t)((rf >> g) & 1u);
+        }
+      }
+      if (ctid == 0) {
+        p.counters[pc.g] = 0;   // leave the counter ready for the next run
+        if (p.write_flags && rf) {
+          atomicAdd(p.stats + 0, (unsigned long long)__popc(rf));
+          const int at = atomicAdd(p.list_state, 1);
+          if (at < p.n_groups) p.flag_list[at] = pc.g;
+        }
+      }
+    }
+  }
+  named_bar_sync(1, kCT);   // shared scratch is free for the next piece
+}
+
+template <typename T, int D, int G, bool UNIFIED>
+__device__ __forceinline__ void run_consumers(const Params& p, Sched s, uint8_t* stages,
+                                              const Layout& L, uint64_t* full, uint64_t* empty,
+                                              uint8_t* smem, int warp, int lane) {
+  using C = Cfg<T, D, G>;
+  constexpr int E = C::kEpl;
+  const uint32_t NS = (uint32_t)p.stages;
+  float* pwarp = reinterpret_cast<float*>(smem + L.pbuf_off) + warp * kTokensPerWarp * G;
+  float* mm = reinterpret_cast<float*>(smem + L.mm_off);
+  float* ml = reinterpret_cast<float*>(smem + L.ml_off);
+  uint32_t* mflag = reinterpret_cast<uint32_t*>(smem + L.mflag_off);
+  float* macc = reinterpret_cast<float*>(smem + L.macc_off);
+  int* misc = reinterpret_cast<int*>(smem + L.misc_off);
+  const int li = lane % C::kLg;
+  const int ctid = warp * 32 + lane;
+  uint32_t k = 0;
+  bool dead = false;
+  Piece pc;
+  while (sched_next(s, p, pc)) {
+    float acc[G][E], den[G], m[G], q[G][E];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      den[g] = 0.f;
+      m[g] = UNIFIED ? p.phi2 : -INFINITY;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        acc[g][e] = 0.f;
+        q[g][e] = 0.f;
+      }
+    }
+    uint32_t fmask = 0;
+    for (int ts = pc.t0, j = 0; ts < pc.t1; ts += kStageTokens, ++j, ++k) {
+      const uint32_t slot = k % NS, ph = (k / NS) & 1u;
+      if (!dead && !mbar_wait(&full[slot], ph)) {
+        dead = true;
+        if (lane == 0) atomicOr(p.status, kStatusTimeout);
+      }
+      const uint8_t* st = stages + slot * L.stage_bytes;
+      if (j == 0) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const uint4 c = *reinterpret_cast<const uint4*>(st + L.q_off + g * C::kRowBytes + li * 16);
+          Elem<T>::to_f32(c, q[g]);
+#pragma unroll
+          for (int e = 0; e < E; ++e) q[g][e] *= p.qscale;
+        }
+      }
+      if (!dead)
+        consume_stage<T, D, G, UNIFIED>(p, st + L.k_off, st + L.v_off, min(kStageTokens, pc.t1 - ts),
+                                        warp, lane, q, acc, den, m, fmask, pwarp);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+    finish_piece<T, D, G, UNIFIED>(p, pc, acc, den, m, fmask, mm, ml, mflag, macc, misc, warp,
+                                   lane, ctid);
+  }
+}
+
+template <typename T, int D, int G, bool UNIFIED>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_split_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmk,
+                        const __grid_constant__ CUtensorMap tmv) {
+  using C = Cfg<T, D, G>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                             ~static_cast<uintptr_t>(127));
+  const Layout L = make_layout(D, G, C::kEs, p.stages, p.batch_smem);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
+  uint64_t* empty = full + p.stages;
+  int* lens = reinterpret_cast<int*>(smem + L.lens_off);
+  int* prefix = reinterpret_cast<int*>(smem + L.prefix_off);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  if (warp == kConsumerWarps && lane == 0) {
+    prefetch_tensormap(&tmk);
+    prefetch_tensormap(&tmv);
+  }
+  // Inputs written by a predecessor launched with programmatic serialization (and, for
+  // the recompute pass, the flagged-group list) are visible after this point.
+  pdl_wait();
+
+  Sched s;
+  s.policy = p.policy;
+  s.P = gridDim.x;
+  s.c = blockIdx.x;
+  s.lens = lens;
+  s.prefix = prefix;
+  s.u = s.u1 = s.W = 0;
+  s.i = s.i1 = 0;
+  s.S = p.num_splits > 0 ? p.num_splits : 1;
+  if (p.policy == kBalanced) {
+    for (int b = tid; b < p.batch; b += blockDim.x) {
+      const int raw = __ldg(p.seq_lens + b);
+      const int n = clamp_len(p, raw);
+      if (n != raw && blockIdx.x == 0) atomicOr(p.status, kStatusBadSeqLen);
+      lens[b] = n;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const int per = (p.batch + 31) / 32;
+      const int beg = min(p.batch, lane * per), end = min(p.batch, beg + per);
+      int local = 0;
+      for (int b = beg; b < end; ++b) local += (lens[b] + p.unit - 1) / p.unit;
+      int incl = local;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int run = incl - local;
+      for (int b = beg; b < end; ++b) {
+        prefix[b] = run;
+        run += (lens[b] + p.unit - 1) / p.unit;
+      }
+      if (lane == 31) prefix[p.batch] = incl;
+    }
+    __syncthreads();
+    s.W = (long long)p.hkv * prefix[p.batch];
+    s.u = (long long)blockIdx.x * s.W / gridDim.x;
+    s.u1 = ((long long)blockIdx.x + 1) * s.W / gridDim.x;
+    // sequences with no tokens have no piece: out = 0, lse = -inf, flag = 0
+    for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
+      if (lens[b] != 0) continue;
+      const long long r0 = (long long)b * p.hq;
+      for (int e = tid; e < p.hq * D; e += blockDim.x) store_out(p.out, r0 * D + e, p.out_dtype, 0.f);
+      for (int h = tid; h < p.hq; h += blockDim.x) {
+        if (p.out_lse) p.out_lse[r0 + h] = -INFINITY;
+        if (p.row_flags && p.write_flags) p.row_flags[r0 + h] = 0;
+      }
+    }
+  } else {
+    long long groups = p.n_groups;
+    if (p.use_list) {
+      const int nf = min(__ldcg(p.list_state), p.n_groups);
+      if (nf <= 0) return;   // nothing was flagged: the recompute pass has no work
+      groups = nf;
+    }
+    const long long ni = groups * s.S;
+    s.i = (long long)blockIdx.x * ni / gridDim.x;
+    s.i1 = ((long long)blockIdx.x + 1) * ni / gridDim.x;
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+
+  uint8_t* stages = smem;
+  if (warp == kConsumerWarps)
+    run_producer<T, D, G>(p, s, stages, L, full, empty, &tmk, &tmv, lane);
+  else
+    run_consumers<T, D, G, UNIFIED>(p, s, stages, L, full, empty, smem, warp, lane);
+
+  if (p.use_list) {
+    // the recompute pass's last CTA resets the flagged list for the next run
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      if (atomicAdd(p.list_state + 1, 1) == (int)gridDim.x - 1) {
+        p.list_state[0] = 0;
+        p.list_state[1] = 0;
+      }
+    }
+  }
+}
+
+template <typename T, int D>
+inline const void* pick_kernel(int G, bool unified) {
+#define DA_CASE(GG)                                                             \
+  case GG:                                                                      \
+    return unified ? (const void*)&decode_split_kernel<T, D, GG, true>          \
+                   : (const void*)&decode_split_kernel<T, D, GG, false>;
+  switch (G) {
+    DA_CASE(1)
+    DA_CASE(2)
+    DA_CASE(4)
+    DA_CASE(8)
+    default:
+      return nullptr;
+  }
+#undef DA_CASE
+}
+
+}  // namespace da

@@ -1,0 +1,12 @@
+// da_kernels_f32.cu -- instantiations of the split-KV kernel for float storage.
+#include "da_kernel.cuh"
+
+namespace da {
+
+const void* kernel_f32(int head_dim, int group, bool unified) {
+  if (head_dim == 64) return pick_kernel<float, 64>(group, unified);
+  if (head_dim == 128) return pick_kernel<float, 128>(group, unified);
+  return nullptr;
+}
+
+}  // namespace da

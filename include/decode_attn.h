@@ -1,0 +1,225 @@
+/*
+ * decode_attn.h -- C ABI of the GB300 (sm_103a) single-query decode-attention library.
+ *
+ * Computes, for every sequence b and query head h of a decode step,
+ *     o[b,h] = softmax(scale * q[b,h] . K_b^T) V_b          (natural exp)
+ *     lse[b,h] = ln sum_t exp(scale * q[b,h] . k_t)
+ * over the first seq_lens[b] tokens of the sequence's KV cache. Sources (page, section):
+ *   - "Flash-Decoding: Mathematical Foundations, Split-KV Parallelism, Online Softmax
+ *     Reduction, and Serving Latency Optimization": "The Single-Token Generation
+ *     Bottleneck" (the operation), "Mathematical Formulation of Split-KV Parallelism"
+ *     (split partials O, m, l, L), "The Rescaling and Online Softmax Reduction Algorithm"
+ *     (exact merge), "Production Implementation Guidelines" (split heuristics).
+ *   - "FlashAttention and inference kernels": "PagedAttention" (block table), "A paged
+ *     decode attention kernel (with GQA)" (cache layout, kernel signature, GQA mapping
+ *     kv_head = h / (H_q / H_kv)), Exercise 3 (one read of a KV head serves its group).
+ *   - "FlashDecoding++: Faster Large Language Model Inference on GPUs": "Asynchronized
+ *     Softmax with Unified Max Value" (Eq. 3, Eq. 4) and "The Overflow Fallback:
+ *     Recomputation" (Fig. 6: range check, synchronised recompute of flagged rows).
+ *
+ * Conventions for every entry point:
+ *   - Device pointers are CUDA device (or managed) addresses on the device that is
+ *     current when the call is made; host pointers are plain host memory.
+ *   - The caller owns every buffer: inputs, outputs and the workspace. The library owns
+ *     only the host-side plan object. decode_attn_run allocates nothing.
+ *   - Return value: DA_OK (0) or a negative DA_ERR_* code; decode_attn_strerror gives a
+ *     message (for DA_ERR_CUDA it includes the CUDA error text of the failing call on
+ *     this thread). No exception crosses the ABI. Argument errors are detected on the
+ *     host before anything is enqueued.
+ *   - Work is enqueued on the given cudaStream_t (NULL = legacy default stream) and the
+ *     call returns without synchronising, unless the problem's `validate` flag is set
+ *     or a stats struct is requested: then the call synchronises the stream and reports
+ *     device-side findings (bad block-table entries, bad lengths, pipeline timeouts).
+ *   - Thread safety: plans are read-only after creation and may be shared between
+ *     threads; one workspace must not be used by two runs that can overlap on the GPU.
+ */
+#ifndef DECODE_ATTN_H
+#define DECODE_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DECODE_ATTN_ABI_VERSION 1
+
+typedef enum { DA_F32 = 0, DA_F16 = 1, DA_BF16 = 2 } da_dtype;
+
+/* DA_SOFTMAX_SYNC: each split runs the online-softmax recurrence with its running
+ *   maximum ("FlashAttention and inference kernels", "FlashAttention: tiling plus online
+ *   softmax"; FlashDecoding++ Eq. 2).
+ * DA_SOFTMAX_UNIFIED: every split exponentiates against the one constant phi =
+ *   unified_max, with no maximum and no rescaling (FlashDecoding++ Eq. 3 and Eq. 4). A
+ *   scaled logit x with x - phi < range_lo or x - phi > range_hi (the interval is
+ *   closed: a value on a bound is in range, as in Fig. 6) flags its row; flagged rows are
+ *   recomputed in DA_SOFTMAX_SYNC mode on the device, in the same call. */
+typedef enum { DA_SOFTMAX_SYNC = 0, DA_SOFTMAX_UNIFIED = 1 } da_softmax_mode;
+
+enum {
+  DA_OK = 0,
+  DA_ERR_INVALID_ARG = -1,          /* a null, misaligned or inconsistent argument */
+  DA_ERR_UNSUPPORTED = -2,          /* head_dim, dtype, group size or page size not built */
+  DA_ERR_WORKSPACE_TOO_SMALL = -3,  /* workspace_bytes below the plan's requirement */
+  DA_ERR_BAD_BLOCK_TABLE = -4,      /* validate: a used block-table entry outside the pool */
+  DA_ERR_CUDA = -5,                 /* a CUDA runtime / driver call failed */
+  DA_ERR_DEVICE_TIMEOUT = -6,       /* validate: a device pipeline wait ran out of time */
+  DA_ERR_BAD_SEQ_LEN = -7           /* validate: seq_lens[b] < 0 or above the capacity */
+};
+
+typedef struct {
+  int batch;                /* B >= 1 sequences */
+  int num_q_heads;          /* H_q */
+  int num_kv_heads;         /* H_kv; H_q % H_kv == 0; group G = H_q / H_kv in {1,2,4,8} */
+  int head_dim;             /* d in {64, 128} */
+  int paged;                /* 1: k/v caches are [num_physical_blocks, page_size, H_kv, d]
+                               addressed through block_table (FlashAttention and inference
+                               kernels, "PagedAttention");
+                               0: k/v caches are [batch, max_seq_len, H_kv, d] */
+  int page_size;            /* paged: tokens per physical block, a power of two in [8, 256] */
+  int max_blocks_per_seq;   /* paged: block_table row length */
+  int num_physical_blocks;  /* paged: pool size; num_physical_blocks * page_size < 2^31 */
+  int max_seq_len;          /* contiguous: token capacity per sequence;
+                               batch * max_seq_len < 2^31 */
+  da_dtype qkv_dtype;       /* storage of q, k_cache and v_cache */
+  da_dtype out_dtype;       /* storage of out (rounded to nearest even from fp32) */
+  da_softmax_mode mode;
+  float unified_max;        /* phi (natural-log units of the scaled logits); UNIFIED only */
+  float range_lo;           /* closed in-range interval on x - phi; range_lo < range_hi */
+  float range_hi;
+  int validate;             /* 1: every run synchronises and reports device findings */
+  int num_sms;              /* 0: plan for the current device's SM count; > 0: plan for
+                               that many SMs without touching CUDA (host-side planning) */
+} da_problem;
+
+typedef struct da_plan da_plan;   /* opaque, host-owned, immutable after creation */
+
+/* What a plan chose (host-side, no CUDA call). */
+typedef struct {
+  int grid_ctas;            /* persistent CTAs per launch */
+  int num_splits;           /* 0: balanced shares (one contiguous share per CTA);
+                               > 0: uniform splits per sequence */
+  int unit_tokens;          /* split boundaries fall on multiples of this many tokens */
+  int stage_tokens;         /* tokens per shared-memory pipeline stage */
+  int stages;               /* pipeline depth */
+  int recompute_splits;     /* uniform splits per flagged group in the recompute pass */
+  int max_splits;           /* largest num_splits a run may ask for with this workspace */
+  size_t workspace_bytes;   /* device workspace the runs need */
+  size_t smem_bytes;        /* dynamic shared memory per CTA */
+} da_plan_info;
+
+/* Filled by decode_attn_run when requested (forces a stream synchronisation). */
+typedef struct {
+  int grid_ctas;
+  int num_splits;           /* as in da_plan_info, for this run */
+  long long rows_flagged;   /* UNIFIED: (b, h) rows whose range check failed */
+  long long splits_flagged; /* UNIFIED: (split, h) partials whose range check failed */
+  int recompute_launched;   /* 1 iff the recompute kernel was enqueued (UNIFIED) */
+} da_stats;
+
+/* Validate a problem and choose the launch (grid, split policy, pipeline) for it.
+ * num_splits: 0 = heuristic (one balanced share of the whole step's KV tokens per
+ * persistent CTA, which splits a sequence exactly when the SMs would otherwise idle:
+ * the Flash-Decoding rule of splitting only when B * H under-fills the GPU, applied to
+ * the work itself); > 0 = exactly that many uniform splits per sequence, each of
+ * roundup(ceil(N_b / num_splits), unit) tokens ("Mathematical Formulation of Split-KV
+ * Parallelism"). *workspace_bytes_out receives the workspace size the runs need.
+ * Owns: *plan_out (free with decode_attn_destroy). Errors: INVALID_ARG, UNSUPPORTED,
+ * CUDA (only when num_sms == 0 and the device query fails). */
+int decode_attn_plan(const da_problem* problem, int num_splits, da_plan** plan_out,
+                     size_t* workspace_bytes_out);
+
+/* Copy what the plan chose into *info. Errors: INVALID_ARG. */
+int decode_attn_plan_info(const da_plan* plan, da_plan_info* info);
+
+/* Zero the workspace's self-cleaning counters. Required once for a new workspace before
+ * its first run (a zero-filled allocation needs no call). Enqueued on `stream`.
+ * Errors: INVALID_ARG, WORKSPACE_TOO_SMALL, CUDA. */
+int decode_attn_workspace_init(const da_plan* plan, void* workspace, size_t workspace_bytes,
+                               void* cuda_stream);
+
+/* Run one decode step.
+ *   q           device, [batch, H_q, d] in qkv_dtype, 16-byte aligned.
+ *   k_cache,    device, layout per problem->paged (see da_problem), qkv_dtype, 16-byte
+ *   v_cache     aligned.
+ *   block_table device int32 [batch, max_blocks_per_seq] when paged (entries for the
+ *               pages a sequence uses must lie in [0, num_physical_blocks); the rest are
+ *               ignored, -1 by convention); must be NULL when contiguous.
+ *   seq_lens    device int32 [batch], 0 <= seq_lens[b] <= capacity (paged:
+ *               max_blocks_per_seq * page_size; contiguous: max_seq_len).
+ *   scale       multiplier of q . k (1/sqrt(d) for standard attention).
+ *   num_splits  -1 = the plan's choice; 0 = balanced shares; > 0 = uniform splits
+ *               (at most the plan's max_splits).
+ *   out         device, [batch, H_q, d] in out_dtype. A sequence with seq_lens[b] == 0
+ *               gets out = 0 ("FlashAttention and inference kernels", Exercise 2 skips
+ *               empty segments; an empty row is this library's extension of it).
+ *   out_lse     nullable device float [batch, H_q]: natural-log log-sum-exp of the
+ *               scaled logits (-inf for an empty sequence).
+ *   row_flags   nullable device uint8 [batch, H_q]: UNIFIED: 1 iff the row's range check
+ *               failed (its out/out_lse then come from the synchronised recompute);
+ *               SYNC: 0.
+ *   workspace   device, at least the plan's workspace_bytes, 256-byte aligned, zeroed
+ *               before first use (decode_attn_workspace_init); left reusable.
+ *   cuda_stream cudaStream_t or NULL.
+ *   stats       nullable; when given the call synchronises and fills it.
+ * Errors: INVALID_ARG, WORKSPACE_TOO_SMALL, CUDA, and with validate (or stats):
+ * BAD_BLOCK_TABLE, BAD_SEQ_LEN, DEVICE_TIMEOUT. A bad block-table entry never makes the
+ * device read outside the cache: the page reads as zeros. */
+int decode_attn_run(const da_plan* plan, const void* q, const void* k_cache,
+                    const void* v_cache, const int32_t* block_table, const int32_t* seq_lens,
+                    float scale, int num_splits, void* out, float* out_lse,
+                    uint8_t* row_flags, void* workspace, size_t workspace_bytes,
+                    void* cuda_stream, da_stats* stats);
+
+/* All arguments of one run, for decode_attn_run_ex. Fields as for decode_attn_run, plus:
+ *   split_event_begin, split_event_end: nullable cudaEvent_t handles recorded on the
+ *   stream immediately before and immediately after the split kernel's launch (before the
+ *   recompute kernel), so a caller can time the split kernel alone with
+ *   cudaEventElapsedTime. Both or neither must be given. */
+typedef struct {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  float scale;
+  int num_splits;
+  void* out;
+  float* out_lse;
+  uint8_t* row_flags;
+  void* workspace;
+  size_t workspace_bytes;
+  void* cuda_stream;
+  da_stats* stats;
+  void* split_event_begin;
+  void* split_event_end;
+} da_run_args;
+
+/* decode_attn_run with its arguments in a struct and optional timing events.
+ * Errors: as decode_attn_run; INVALID_ARG also when only one event is given. */
+int decode_attn_run_ex(const da_plan* plan, const da_run_args* args);
+
+/* Synchronise `stream`, then read and clear the device findings recorded in the
+ * workspace by earlier runs. Returns DA_OK or the first finding's DA_ERR_* code. */
+int decode_attn_check_status(const da_plan* plan, void* workspace, void* cuda_stream);
+
+/* Test hook: the element offset (into k_cache / v_cache) from which the device reads
+ * token t of (sequence b, KV head kvh), computed by the same device code the kernel's
+ * loads use. offsets_out: device int64 [batch, H_kv, T] with T = max_blocks_per_seq *
+ * page_size (paged) or max_seq_len (contiguous); -1 for t >= seq_lens[b] and for a
+ * block-table entry outside the pool. Enqueued on `stream`. Errors: INVALID_ARG, CUDA. */
+int decode_attn_debug_gather(const da_plan* plan, const int32_t* block_table,
+                             const int32_t* seq_lens, int64_t* offsets_out, void* cuda_stream);
+
+void decode_attn_destroy(da_plan* plan);
+
+const char* decode_attn_strerror(int code);
+
+int decode_attn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DECODE_ATTN_H */
