@@ -21,6 +21,7 @@ namespace da {
 const void* kernel_f32(int head_dim, int group, bool unified);
 const void* kernel_f16(int head_dim, int group, bool unified);
 const void* kernel_bf16(int head_dim, int group, bool unified);
+const void* merge_kernel_ptr();
 
 // The element offset the kernel reads token t of (b, kvh) from: the same token_row() the
 // producer warp uses for its TMA box coordinates.
@@ -57,7 +58,7 @@ struct da_plan {
   int stages, batch_smem;
   size_t smem_bytes;
   long long slots;
-  size_t off_counters, off_list, off_list_state, off_status, off_stats;
+  size_t off_counters, off_list, off_list_state, off_status, off_stats, off_desc;
   size_t off_part_flags, off_part_l, off_part_o, zero_bytes, ws_bytes;
 };
 
@@ -125,6 +126,11 @@ int ensure_smem_attr(const void* fn, size_t smem) {
   if (g_attr_done.count({dev, fn})) return DA_OK;
   e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  // Every kernel of a run asks for the maximal shared-memory carveout, so that the merge
+  // kernel's CTAs can share an SM with the split kernel's instead of waiting for a reconfigure.
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(carveout)");
   (void)smem;
   g_attr_done.insert({dev, fn});
   return DA_OK;
@@ -187,6 +193,7 @@ void fill_common(const da_plan& pl, Params& k, const int32_t* block_table,
     k.part_flags = reinterpret_cast<uint32_t*>(w + pl.off_part_flags);
     k.part_l = reinterpret_cast<float*>(w + pl.off_part_l);
     k.part_o = reinterpret_cast<float*>(w + pl.off_part_o);
+    k.desc = reinterpret_cast<int2*>(w + pl.off_desc);
   }
   k.batch = p.batch;
   k.hq = p.num_q_heads;
@@ -265,6 +272,12 @@ int decode_attn_plan(const da_problem* problem, int num_splits, da_plan** plan_o
   const long long w_max = (long long)pl->n_groups * units_max;
   pl->batch_smem = p.batch <= kMaxBatchSmem ? p.batch : 0;
 
+  // the merge stages one weight per (split, head) in 8 * d * G floats of shared memory
+  const int split_cap = kConsumerWarps * p.head_dim;
+  if (num_splits > split_cap) {
+    delete pl;
+    return DA_ERR_UNSUPPORTED;
+  }
   if (num_splits > 0) {
     pl->policy = kUniform;
     pl->num_splits = num_splits;
@@ -287,7 +300,7 @@ int decode_attn_plan(const da_problem* problem, int num_splits, da_plan** plan_o
   const long long need_uniform =
       (long long)pl->n_groups * std::max(pl->recompute_splits, pl->policy == kUniform ? pl->num_splits : 1);
   pl->slots = std::max<long long>((long long)sms + pl->n_groups, need_uniform);
-  pl->max_splits = (int)std::min<long long>(1 << 20, pl->slots / pl->n_groups);
+  pl->max_splits = (int)std::min<long long>(split_cap, pl->slots / pl->n_groups);
 
   // deepest pipeline that fits the per-CTA shared memory limit
   pl->stages = 0;
@@ -315,6 +328,8 @@ int decode_attn_plan(const da_problem* problem, int num_splits, da_plan** plan_o
   pl->off_stats = off + 16;
   off = align256(off + 32);
   pl->zero_bytes = off;
+  pl->off_desc = off;
+  off = align256(off + (size_t)pl->n_groups * 8);
   pl->off_part_flags = off;
   off = align256(off + (size_t)pl->slots * 4);
   pl->off_part_l = off;
@@ -473,25 +488,62 @@ int decode_attn_run_ex(const da_plan* plan, const da_run_args* args) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(split_event_end)");
   }
 
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  {
+    // Merge of the groups split into several pieces, as a programmatic dependent without
+    // shared memory: its CTAs wait beside the split kernel's and start when its writes land.
+    MergeParams mp;
+    std::memset(&mp, 0, sizeof mp);
+    mp.out = out;
+    mp.out_lse = out_lse;
+    mp.row_flags = row_flags;
+    mp.part_o = kp.part_o;
+    mp.part_l = kp.part_l;
+    mp.part_flags = kp.part_flags;
+    mp.desc = kp.desc;
+    mp.flag_list = kp.flag_list;
+    mp.list_state = kp.list_state;
+    mp.stats = kp.stats;
+    mp.n_groups = pl.n_groups;
+    mp.rows_per_group = pl.group;
+    mp.head_dim = p.head_dim;
+    mp.out_dtype = p.out_dtype;
+    mp.write_flags = 1;
+    const long long items = (long long)pl.n_groups * pl.group * (p.head_dim / 32);
+    cudaLaunchConfig_t mcfg = {};
+    mcfg.gridDim = dim3((unsigned)std::max<long long>(
+        1, std::min<long long>((items + 3) / 4, (long long)pl.num_sms * 4)));
+    mcfg.blockDim = dim3(128);
+    mcfg.dynamicSmemBytes = 0;
+    mcfg.stream = stream;
+    mcfg.attrs = pdl;
+    mcfg.numAttrs = 1;
+    void* margs[1] = {&mp};
+    rc = ensure_smem_attr(merge_kernel_ptr(), 0);
+    if (rc != DA_OK) return rc;
+    e = cudaLaunchKernelExC(&mcfg, merge_kernel_ptr(), margs);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the merge kernel");
+  }
+
   if (unified) {
     // Synchronised recompute of flagged groups ("The Overflow Fallback: Recomputation").
-    // Always enqueued, as a programmatic dependent of the split kernel, so that no host
-    // round trip is needed; it exits at once when nothing was flagged.
+    // Always enqueued, as a programmatic dependent of the merge, so that no host round trip
+    // is needed; it exits at once when nothing was flagged. Its pieces merge in-kernel.
     Params rp = kp;
     rp.policy = kUniform;
     rp.num_splits = pl.recompute_splits;
     rp.use_list = 1;
     rp.write_flags = 0;
+    rp.inline_merge = 1;
     const void* rfn = kernel_for(pl, false);
     rc = ensure_smem_attr(rfn, pl.smem_bytes);
     if (rc != DA_OK) return rc;
     cudaLaunchConfig_t rcfg = cfg;
     rcfg.gridDim = dim3((unsigned)std::min<long long>(
         pl.num_sms, (long long)pl.n_groups * pl.recompute_splits));
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    rcfg.attrs = attr;
+    rcfg.attrs = pdl;
     rcfg.numAttrs = 1;
     void* rargs[3] = {&rp, &tmk, &tmv};
     e = cudaLaunchKernelExC(&rcfg, rfn, rargs);

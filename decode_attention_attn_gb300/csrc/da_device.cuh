@@ -63,6 +63,23 @@ struct Params {
   int batch_smem;                // lengths held in smem (balanced) or 0
   float qscale;                  // scale * log2(e): logits come out in log2 units
   float phi2, lo2, hi2;          // unified constant and range bounds, log2 units
+  int2* desc;                    // [n_groups] (first partial slot, pieces) of each group
+  int inline_merge;              // 1: the last piece of a group merges it (recompute pass)
+};
+
+// Launch parameters of the merge kernel (one warp per (group, row, 32-wide d chunk)).
+struct MergeParams {
+  void* out;
+  float* out_lse;
+  uint8_t* row_flags;
+  const float* part_o;
+  const float* part_l;
+  const uint32_t* part_flags;
+  const int2* desc;
+  int32_t* flag_list;
+  int32_t* list_state;
+  unsigned long long* stats;
+  int n_groups, rows_per_group, head_dim, out_dtype, write_flags;
 };
 
 // ---- shared-memory layout (host and device compute it identically) ------------------------
@@ -86,7 +103,7 @@ __host__ __device__ inline Layout make_layout(int D, int G, int es, int stages, 
   off += 2u * stages * 8u;
   off = align_up(off, 16);
   L.pbuf_off = off;
-  off += (uint32_t)kConsumerWarps * kTokensPerWarp * G * 4u;
+  off += (uint32_t)kConsumerWarps * kTokensPerWarp * G * 8u;   // (p, p) pairs
   L.mm_off = off;
   off += (uint32_t)kConsumerWarps * G * 4u;
   L.ml_off = off;

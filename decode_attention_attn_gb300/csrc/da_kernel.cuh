@@ -252,25 +252,48 @@ __device__ __forceinline__ void run_producer(const Params& p, Sched s, uint8_t* 
   }
 }
 
-// ---- consumer warps: one stage ----------------------------------------------------------
+// ---- consumer warps ---------------------------------------------------------------------
+// Per-lane constants of the logit layout after the transpose-reduce.
+template <typename T, int D, int G>
+struct LaneMap {
+  using C = Cfg<T, D, G>;
+  int lg, li, row0;              // lane group, lane in group, first stage row of the group
+  int j[C::kNv], g[C::kNv];      // token (within the lane group) and head of each logit
+  bool writer;                   // the lane that publishes a replicated logit
+  __device__ __forceinline__ LaneMap(int warp, int lane) {
+    lg = lane / C::kLg;
+    li = lane % C::kLg;
+    row0 = warp * kTokensPerWarp + lg * C::kT;
+#pragma unroll
+    for (int i = 0; i < C::kNv; ++i) {
+      const int idx = C::kV >= C::kLg ? li * C::kNv + i : li / C::kRep;
+      j[i] = idx / G;
+      g[i] = idx % G;
+    }
+    writer = (li % C::kRep) == 0;
+  }
+  __device__ __forceinline__ int idx(int i) const { return j[i] * G + g[i]; }
+};
+
+// One stage: the warp's 8 rows. p values are published to shared memory as (p, p) pairs so
+// that P . V takes its packed-FMA operands straight from a 16-byte load.
 template <typename T, int D, int G, bool UNIFIED>
-__device__ __forceinline__ void consume_stage(const Params& p, const uint8_t* ks,
-                                              const uint8_t* vs, int n, int warp, int lane,
+__device__ __forceinline__ void consume_stage(const Params& p, const LaneMap<T, D, G>& lm,
+                                              const uint8_t* ks, const uint8_t* vs, int n,
                                               const float (&q)[G][Cfg<T, D, G>::kEpl],
                                               float (&acc)[G][Cfg<T, D, G>::kEpl],
-                                              float (&den)[G], float (&m)[G], uint32_t& fmask,
-                                              float* pwarp) {
+                                              float (&dl)[Cfg<T, D, G>::kNv], float (&m)[G],
+                                              uint32_t& fmask, float2* pwarp) {
   using C = Cfg<T, D, G>;
   constexpr int E = C::kEpl;
-  const int lg = lane / C::kLg, li = lane % C::kLg;
-  const int row0 = warp * kTokensPerWarp + lg * C::kT;
-  float* pw = pwarp + lg * C::kV;
+  float2* pw = pwarp + lm.lg * C::kV;
 
   // q . k for the lane group's rows and all G heads: partial sums over this lane's chunk
   float part[C::kV];
 #pragma unroll
   for (int j = 0; j < C::kT; ++j) {
-    const uint4 c = *reinterpret_cast<const uint4*>(ks + (row0 + j) * C::kRowBytes + li * 16);
+    const uint4 c =
+        *reinterpret_cast<const uint4*>(ks + (lm.row0 + j) * C::kRowBytes + lm.li * 16);
     float kf[E];
     Elem<T>::to_f32(c, kf);
 #pragma unroll
@@ -282,33 +305,26 @@ __device__ __forceinline__ void consume_stage(const Params& p, const uint8_t* ks
       part[j * G + g] = s2.x + s2.y;
     }
   }
-  Reduce<C::kV, C::kLg / 2>::run(part, lane);
+  Reduce<C::kV, C::kLg / 2>::run(part, lm.li);
 
-  // this lane's complete logits: index = row * G + head
-  int gi[C::kNv];
   bool valid[C::kNv];
 #pragma unroll
-  for (int i = 0; i < C::kNv; ++i) {
-    const int idx = C::kV >= C::kLg ? li * C::kNv + i : li / C::kRep;
-    gi[i] = idx % G;
-    valid[i] = row0 + idx / G < n;
-  }
-  const bool writer = (li % C::kRep) == 0;
+  for (int i = 0; i < C::kNv; ++i) valid[i] = lm.row0 + lm.j[i] < n;
 
   if constexpr (UNIFIED) {
 #pragma unroll
     for (int i = 0; i < C::kNv; ++i) {
       const float s = part[i];
       const float pr = valid[i] ? fast_exp2(s - p.phi2) : 0.f;
-      if (valid[i] && (s < p.lo2 || s > p.hi2)) fmask |= 1u << gi[i];
-      const int idx = C::kV >= C::kLg ? li * C::kNv + i : li / C::kRep;
-      if (writer) pw[idx] = pr;
+      if (valid[i] && (s < p.lo2 || s > p.hi2)) fmask |= 1u << lm.g[i];
+      dl[i] += pr;
+      if (lm.writer) pw[lm.idx(i)] = make_float2(pr, pr);
     }
   } else {
 #pragma unroll
     for (int i = 0; i < C::kNv; ++i) {
-      const int idx = C::kV >= C::kLg ? li * C::kNv + i : li / C::kRep;
-      if (writer) pw[idx] = valid[i] ? part[i] : -INFINITY;
+      const float s = valid[i] ? part[i] : -INFINITY;
+      if (lm.writer) pw[lm.idx(i)] = make_float2(s, s);
     }
     __syncwarp();
     // per-head maximum over the warp's 8 rows of this stage, then the online update
@@ -318,26 +334,29 @@ __device__ __forceinline__ void consume_stage(const Params& p, const uint8_t* ks
 #pragma unroll
     for (int r = 0; r < kTokensPerWarp; ++r)
 #pragma unroll
-      for (int g = 0; g < G; ++g) tm[g] = fmaxf(tm[g], pwarp[r * G + g]);
+      for (int g = 0; g < G; ++g) tm[g] = fmaxf(tm[g], pwarp[r * G + g].x);
+    float alpha[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       const float mn = fmaxf(m[g], tm[g]);
-      const float alpha = mn == -INFINITY ? 1.f : fast_exp2(m[g] - mn);
+      alpha[g] = mn == -INFINITY ? 1.f : fast_exp2(m[g] - mn);
       m[g] = mn;
-      den[g] *= alpha;
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[g][e] *= alpha;
+      for (int e = 0; e < E; ++e) acc[g][e] *= alpha[g];
     }
     __syncwarp();
 #pragma unroll
     for (int i = 0; i < C::kNv; ++i) {
-      float mg = m[0];
+      float mg = m[0], ag = alpha[0];
 #pragma unroll
       for (int g = 1; g < G; ++g)
-        if (gi[i] == g) mg = m[g];
+        if (lm.g[i] == g) {
+          mg = m[g];
+          ag = alpha[g];
+        }
       const float pr = valid[i] ? fast_exp2(part[i] - mg) : 0.f;
-      const int idx = C::kV >= C::kLg ? li * C::kNv + i : li / C::kRep;
-      if (writer) pw[idx] = pr;
+      dl[i] = dl[i] * ag + pr;
+      if (lm.writer) pw[lm.idx(i)] = make_float2(pr, pr);
     }
   }
   __syncwarp();
@@ -345,19 +364,28 @@ __device__ __forceinline__ void consume_stage(const Params& p, const uint8_t* ks
   // P . V: every lane of the group accumulates its chunk of d for all heads
 #pragma unroll
   for (int j = 0; j < C::kT; ++j) {
-    if (row0 + j < n) {
-      const uint4 c = *reinterpret_cast<const uint4*>(vs + (row0 + j) * C::kRowBytes + li * 16);
+    if (lm.row0 + j < n) {
+      const uint4 c =
+          *reinterpret_cast<const uint4*>(vs + (lm.row0 + j) * C::kRowBytes + lm.li * 16);
       float vf[E];
       Elem<T>::to_f32(c, vf);
+      float2 pp[G];
+      if constexpr (G == 1) {
+        pp[0] = pw[j];
+      } else {
+#pragma unroll
+        for (int g = 0; g < G; g += 2) {
+          const float4 two = *reinterpret_cast<const float4*>(pw + j * G + g);
+          pp[g] = make_float2(two.x, two.y);
+          pp[g + 1] = make_float2(two.z, two.w);
+        }
+      }
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const float pr = pw[j * G + g];
-        den[g] += pr;
-        const float2 pp = make_float2(pr, pr);
 #pragma unroll
         for (int e = 0; e < E; e += 2) {
           float2 a2 = make_float2(acc[g][e], acc[g][e + 1]);
-          ffma2(a2, pp, make_float2(vf[e], vf[e + 1]));
+          ffma2(a2, pp[g], make_float2(vf[e], vf[e + 1]));
           acc[g][e] = a2.x;
           acc[g][e + 1] = a2.y;
         }
@@ -370,33 +398,42 @@ __device__ __forceinline__ void consume_stage(const Params& p, const uint8_t* ks
 // ---- consumer warps: end of a piece ---------------------------------------------------
 template <typename T, int D, int G, bool UNIFIED>
 __device__ __forceinline__ void finish_piece(const Params& p, const Piece& pc,
+                                             const LaneMap<T, D, G>& lm,
                                              float (&acc)[G][Cfg<T, D, G>::kEpl],
-                                             float (&den)[G], const float (&m)[G],
-                                             uint32_t fmask, float* mm, float* ml,
-                                             uint32_t* mflag, float* macc, int* misc, int warp,
-                                             int lane, int ctid) {
+                                             const float (&dl)[Cfg<T, D, G>::kNv],
+                                             const float (&m)[G], uint32_t fmask, float* mm,
+                                             float* ml, uint32_t* mflag, float* macc, int* misc,
+                                             int warp, int lane, int ctid) {
   using C = Cfg<T, D, G>;
   constexpr int E = C::kEpl;
   constexpr int kCT = kConsumerWarps * 32;
   constexpr float kLn2 = 0.6931471805599453f;
-  const int lg = lane / C::kLg, li = lane % C::kLg;
 
+  // the warp's denominators: each head's p values are spread over the lanes holding it
+  float den[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < C::kNv; ++i)
+      if (lm.writer && lm.g[i] == g) s += dl[i];
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    den[g] = s;
+  }
   // combine the warp's lane groups (same d-chunk, disjoint rows)
 #pragma unroll
-  for (int o = C::kLg; o < 32; o <<= 1) {
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      den[g] += __shfl_xor_sync(0xffffffffu, den[g], o);
-#pragma unroll
-      for (int e = 0; e < E; ++e) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], o);
-    }
-  }
-  const uint32_t fm = __reduce_or_sync(0xffffffffu, fmask);
-  if (lg == 0) {
+  for (int o = C::kLg; o < 32; o <<= 1)
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
-      for (int e = 0; e < E; ++e) macc[(warp * G + g) * D + li * E + e] = acc[g][e];
+      for (int e = 0; e < E; ++e) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], o);
+  const uint32_t fm = __reduce_or_sync(0xffffffffu, fmask);
+  if (lm.lg == 0) {
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int e = 0; e < E; ++e) macc[(warp * G + g) * D + lm.li * E + e] = acc[g][e];
   }
   if (lane == 0) {
 #pragma unroll
@@ -453,47 +490,85 @@ __device__ __forceinline__ void finish_piece(const Params& p, const Piece& pc,
     }
   }
 
+  if (!p.inline_merge && ctid == 0 && pc.slot == pc.slot_base)
+    p.desc[pc.g] = make_int2(pc.slot_base, direct ? 1 : pc.nslots);   // for the merge kernel
+
   if (!direct) {
     if (ctid == 0) __stcg(p.part_flags + pc.slot, fl);
+  }
+  if (!direct && p.inline_merge) {
     __threadfence();
     named_bar_sync(1, kCT);
     if (ctid == 0) {
       const int old = atomicAdd(p.counters + pc.g, 1);
       misc[0] = old == pc.nslots - 1;
+      misc[1] = 0;
     }
     named_bar_sync(1, kCT);
     if (misc[0]) {
-      // last piece of the group: exact log-sum-exp merge of all its partials
+      // Last piece of the group: exact log-sum-exp merge of all its partials. Every pass is
+      // parallel over slots so the merge pays the L2 latency a few times, not per slot.
       __threadfence();
+      const int S = pc.nslots;
+      float* wts = macc;              // [S, G] weights (scratch reused; S <= 8 * D)
+      float* hsum = mm;               // [G] sum of weights
+      float* hmax = ml;               // [G] maximum partial LSE
+      const float* pl = p.part_l + (long long)pc.slot_base * G;
+      for (int i = ctid; i < S * G; i += kCT) wts[i] = __ldcg(pl + i);
       uint32_t rf = 0;
-      for (int s = 0; s < pc.nslots; ++s) rf |= __ldcg(p.part_flags + pc.slot_base + s);
+      for (int s = ctid; s < S; s += kCT) rf |= __ldcg(p.part_flags + pc.slot_base + s);
+      rf = __reduce_or_sync(0xffffffffu, rf);
+      if (lane == 0 && rf) atomicOr(reinterpret_cast<unsigned int*>(misc + 1), rf);
+      named_bar_sync(1, kCT);
+      if (warp < G) {
+        const int g = warp;
+        float M = -INFINITY;
+        for (int s = lane; s < S; s += 32) M = fmaxf(M, wts[s * G + g]);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float sum = 0.f;
+        for (int s = lane; s < S; s += 32) {
+          const float L = wts[s * G + g];
+          const float f = L > -INFINITY ? fast_exp2(L - M) : 0.f;
+          wts[s * G + g] = f;
+          sum += f;
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (lane == 0) {
+          hsum[g] = sum;
+          hmax[g] = M;
+        }
+      }
+      named_bar_sync(1, kCT);
+      const float* po = p.part_o + (long long)pc.slot_base * G * D;
       for (int e = ctid; e < G * D; e += kCT) {
         const int g = e / D, d = e - (e / D) * D;
-        float Lm = -INFINITY;
-        for (int s = 0; s < pc.nslots; ++s)
-          Lm = fmaxf(Lm, __ldcg(p.part_l + (long long)(pc.slot_base + s) * G + g));
-        float num = 0.f, sum = 0.f;
-        if (Lm > -INFINITY) {
-          for (int s = 0; s < pc.nslots; ++s) {
-            const float Ls = __ldcg(p.part_l + (long long)(pc.slot_base + s) * G + g);
-            if (Ls > -INFINITY) {
-              const float f = fast_exp2(Ls - Lm);
-              sum += f;
-              num += f * __ldcg(p.part_o + ((long long)(pc.slot_base + s) * G + g) * D + d);
-            }
-          }
+        float num = 0.f;
+        int s = 0;
+        for (; s + 4 <= S; s += 4) {
+          const float o0 = __ldcg(po + (long long)(s + 0) * G * D + e);
+          const float o1 = __ldcg(po + (long long)(s + 1) * G * D + e);
+          const float o2 = __ldcg(po + (long long)(s + 2) * G * D + e);
+          const float o3 = __ldcg(po + (long long)(s + 3) * G * D + e);
+          num += wts[(s + 0) * G + g] * o0 + wts[(s + 1) * G + g] * o1 +
+                 wts[(s + 2) * G + g] * o2 + wts[(s + 3) * G + g] * o3;
         }
+        for (; s < S; ++s) num += wts[s * G + g] * __ldcg(po + (long long)s * G * D + e);
+        const float sum = hsum[g];
         const float o = sum > 0.f ? num / sum : 0.f;
         store_out(p.out, (row0 + g) * D + d, p.out_dtype, o);
         if (d == 0) {
-          if (p.out_lse) p.out_lse[row0 + g] = sum > 0.f ? (Lm + fast_log2(sum)) * kLn2 : -INFINITY;
-          if (p.row_flags && p.write_flags) p.row_flags[row0 + g] = (uint8_t)((rf >> g) & 1u);
+          if (p.out_lse) p.out_lse[row0 + g] = sum > 0.f ? (hmax[g] + fast_log2(sum)) * kLn2 : -INFINITY;
+          if (p.row_flags && p.write_flags)
+            p.row_flags[row0 + g] = (uint8_t)((((uint32_t)misc[1]) >> g) & 1u);
         }
       }
       if (ctid == 0) {
         p.counters[pc.g] = 0;   // leave the counter ready for the next run
-        if (p.write_flags && rf) {
-          atomicAdd(p.stats + 0, (unsigned long long)__popc(rf));
+        const uint32_t rfa = (uint32_t)misc[1];
+        if (p.write_flags && rfa) {
+          atomicAdd(p.stats + 0, (unsigned long long)__popc(rfa));
           const int at = atomicAdd(p.list_state, 1);
           if (at < p.n_groups) p.flag_list[at] = pc.g;
         }
@@ -510,22 +585,21 @@ __device__ __forceinline__ void run_consumers(const Params& p, Sched s, uint8_t*
   using C = Cfg<T, D, G>;
   constexpr int E = C::kEpl;
   const uint32_t NS = (uint32_t)p.stages;
-  float* pwarp = reinterpret_cast<float*>(smem + L.pbuf_off) + warp * kTokensPerWarp * G;
+  float2* pwarp = reinterpret_cast<float2*>(smem + L.pbuf_off) + warp * kTokensPerWarp * G;
   float* mm = reinterpret_cast<float*>(smem + L.mm_off);
   float* ml = reinterpret_cast<float*>(smem + L.ml_off);
   uint32_t* mflag = reinterpret_cast<uint32_t*>(smem + L.mflag_off);
   float* macc = reinterpret_cast<float*>(smem + L.macc_off);
   int* misc = reinterpret_cast<int*>(smem + L.misc_off);
-  const int li = lane % C::kLg;
+  const LaneMap<T, D, G> lm(warp, lane);
   const int ctid = warp * 32 + lane;
   uint32_t k = 0;
   bool dead = false;
   Piece pc;
   while (sched_next(s, p, pc)) {
-    float acc[G][E], den[G], m[G], q[G][E];
+    float acc[G][E], dl[C::kNv], m[G], q[G][E];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      den[g] = 0.f;
       m[g] = UNIFIED ? p.phi2 : -INFINITY;
 #pragma unroll
       for (int e = 0; e < E; ++e) {
@@ -533,6 +607,8 @@ __device__ __forceinline__ void run_consumers(const Params& p, Sched s, uint8_t*
         q[g][e] = 0.f;
       }
     }
+#pragma unroll
+    for (int i = 0; i < C::kNv; ++i) dl[i] = 0.f;
     uint32_t fmask = 0;
     for (int ts = pc.t0, j = 0; ts < pc.t1; ts += kStageTokens, ++j, ++k) {
       const uint32_t slot = k % NS, ph = (k / NS) & 1u;
@@ -544,20 +620,22 @@ __device__ __forceinline__ void run_consumers(const Params& p, Sched s, uint8_t*
       if (j == 0) {
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          const uint4 c = *reinterpret_cast<const uint4*>(st + L.q_off + g * C::kRowBytes + li * 16);
+          const uint4 c =
+              *reinterpret_cast<const uint4*>(st + L.q_off + g * C::kRowBytes + lm.li * 16);
           Elem<T>::to_f32(c, q[g]);
 #pragma unroll
           for (int e = 0; e < E; ++e) q[g][e] *= p.qscale;
         }
       }
       if (!dead)
-        consume_stage<T, D, G, UNIFIED>(p, st + L.k_off, st + L.v_off, min(kStageTokens, pc.t1 - ts),
-                                        warp, lane, q, acc, den, m, fmask, pwarp);
+        consume_stage<T, D, G, UNIFIED>(p, lm, st + L.k_off, st + L.v_off,
+                                        min(kStageTokens, pc.t1 - ts), q, acc, dl, m, fmask,
+                                        pwarp);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
     }
-    finish_piece<T, D, G, UNIFIED>(p, pc, acc, den, m, fmask, mm, ml, mflag, macc, misc, warp,
-                                   lane, ctid);
+    finish_piece<T, D, G, UNIFIED>(p, pc, lm, acc, dl, m, fmask, mm, ml, mflag, macc, misc,
+                                   warp, lane, ctid);
   }
 }
 
@@ -639,6 +717,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.out_lse) p.out_lse[r0 + h] = -INFINITY;
         if (p.row_flags && p.write_flags) p.row_flags[r0 + h] = 0;
       }
+      for (int kv = tid; kv < p.hkv; kv += blockDim.x)
+        if (!p.inline_merge) p.desc[(long long)b * p.hkv + kv] = make_int2(0, 0);
     }
   } else {
     long long groups = p.n_groups;

@@ -83,7 +83,10 @@ def paged64():
 def test_paged_batch64_bf16(paged64, mode):
     dev, (ref, ref_lse, ref_flag, margin) = paged64
     out, lse, flags = _check(dev, ref, ref_lse, mode, where="paged b64 heuristic")
+    _check(dev, ref, ref_lse, mode, out_dtype="f32", where="paged b64 fp32-out")
     _check(dev, ref, ref_lse, mode, num_splits=4, plan_splits=4, where="paged b64 S=4")
+    _check(dev, ref, ref_lse, mode, num_splits=4, plan_splits=4, out_dtype="f32",
+           where="paged b64 S=4 fp32-out")
     if mode == "unified":
         assert _parity.margin_ok(margin).all()
         assert np.array_equal(flags.cpu().numpy().ravel(), ref_flag)
@@ -101,6 +104,8 @@ def test_unified_stress_128k():
     assert np.array_equal(got_flags, ref_flag)
     assert st.rows_flagged == int(ref_flag.sum()) and st.recompute_launched == 1
     assert st.splits_flagged >= 1
+    out32, _, _ = _parity.run_gpu(dev, mode="unified", out_dtype="f32")
+    _parity.compare(out32, ref.reshape(out32.shape), "f32", where="stress unified fp32-out")
     out_s, lse_s, flags_s = _parity.run_gpu(dev, mode="sync")
     _parity.compare(out_s, ref.reshape(out_s.shape), "bf16", where="stress sync")
     assert not flags_s.cpu().numpy().any()
@@ -125,8 +130,9 @@ def test_edge_sweep(dtype, head_dim, group):
         for mode in ("sync", "unified"):
             ns = (0, 1, 3, 7)[case % 4]
             case += 1
-            _check(dev, ref, ref_lse, mode, num_splits=ns, plan_splits=ns,
-                   where=f"edge {dtype} d{head_dim} G{group} paged={paged} S={ns}")
+            for od in ((dtype, "f32") if dtype != "f32" else ("f32",)):
+                _check(dev, ref, ref_lse, mode, out_dtype=od, num_splits=ns, plan_splits=ns,
+                       where=f"edge {dtype} d{head_dim} G{group} paged={paged} S={ns}")
 
 
 @pytest.mark.parametrize("page_size", [8, 16, 32, 64, 128])
@@ -138,8 +144,9 @@ def test_page_sizes(page_size):
     ref, ref_lse, _, _ = _parity.run_oracle(inp)
     for mode in ("sync", "unified"):
         for ns in (0, 5):
-            _check(dev, ref, ref_lse, mode, num_splits=ns, plan_splits=ns,
-                   where=f"page {page_size} S={ns}")
+            for od in ("bf16", "f32"):
+                _check(dev, ref, ref_lse, mode, out_dtype=od, num_splits=ns, plan_splits=ns,
+                       where=f"page {page_size} S={ns}")
 
 
 # ---- integer exactness: gather offsets --------------------------------------------------------
