@@ -54,6 +54,17 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(values, device="cpu"):
+    """Element-wise maximum of per-rank timings over the process group (identity on one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -273,11 +284,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     kern_ms = sum(s.elapsed_ms(e) for s, e in zip(ks, ke)) / args.steps
 
-    ms = ms_local
-    if world > 1:
-        t = torch.tensor([ms_local, kern_ms], device=dev_name)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, kern_ms = float(t[0]), float(t[1])
+    ms, kern_ms = max_over_ranks([ms_local, kern_ms], dev_name)
 
     # ---- end to end: pinned host inputs -> device -> run -> host results ----
     e2e = None
@@ -311,10 +318,7 @@ def run_ours(args):
                 ee[j].record(stream)
             stream.synchronize()
         e2e_ms = sum(s.elapsed_time(e) for s, e in zip(es, ee)) / e_steps
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev_name)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t[0])
+        e2e_ms = max_over_ranks([e2e_ms], dev_name)[0]
         e2e = {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": round(e2e_ms, 4)}
