@@ -126,6 +126,19 @@ int ensure_smem_attr(const void* fn, size_t smem) {
   if (g_attr_done.count({dev, fn})) return DA_OK;
   e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  if (smem > 0) {
+    // The split kernels redistribute registers with setmaxnreg; that is only safe when every
+    // thread was launched with kLaunchRegs registers.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, fn);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes");
+    if (fa.numRegs != kLaunchRegs || fa.maxThreadsPerBlock < kThreads) {
+      g_cuda_error = "split kernel built with " + std::to_string(fa.numRegs) +
+                     " registers per thread; the register split needs " +
+                     std::to_string(kLaunchRegs);
+      return DA_ERR_CUDA;
+    }
+  }
   // Every kernel of a run asks for the maximal shared-memory carveout, so that the merge
   // kernel's CTAs can share an SM with the split kernel's instead of waiting for a reconfigure.
   e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -150,8 +163,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [tokens, Hkv, D] view of a K or V cache; one box = box_tokens rows of one KV head.
-int make_kv_map(const da_plan& pl, const void* base, CUtensorMap* map) {
+// [tokens, Hkv, D] view of a K or V cache; one box = box_tokens rows of one KV head. The
+// tensor-core kernels read the tile with ldmatrix and need the 128-byte swizzle, whose rows
+// are at most 128 bytes: for them the view is 4-D, [tokens, Hkv, D / 64, 64].
+int make_kv_map(const da_plan& pl, const void* base, bool swizzled, CUtensorMap* map) {
   auto fn = encode_fn();
   if (!fn) {
     g_cuda_error = "cuTensorMapEncodeTiled is not available from the driver";
@@ -167,9 +182,23 @@ int make_kv_map(const da_plan& pl, const void* base, CUtensorMap* map) {
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   const CUtensorMapDataType dt =
       pl.es == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
-  const CUresult r = fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r;
+  if (swizzled) {
+    const cuuint64_t dims4[4] = {64u, (cuuint64_t)p.head_dim / 64u, (cuuint64_t)p.num_kv_heads,
+                                 tokens};
+    const cuuint64_t strides4[3] = {64u * pl.es, (cuuint64_t)p.head_dim * pl.es,
+                                    (cuuint64_t)p.num_kv_heads * p.head_dim * pl.es};
+    const cuuint32_t box4[4] = {64u, (cuuint32_t)p.head_dim / 64u, 1u,
+                                (cuuint32_t)pl.box_tokens};
+    const cuuint32_t estr4[4] = {1u, 1u, 1u, 1u};
+    r = fn(map, dt, 4, const_cast<void*>(base), dims4, strides4, box4, estr4,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    r = fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   if (r != CUDA_SUCCESS) {
     g_cuda_error = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string((int)r);
     return DA_ERR_CUDA;
@@ -435,9 +464,10 @@ int decode_attn_run_ex(const da_plan* plan, const da_run_args* args) {
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
   const bool unified = p.mode == DA_SOFTMAX_UNIFIED;
 
+  const bool mma = uses_mma(pl.es, p.qkv_dtype == DA_BF16, pl.group, unified);
   CUtensorMap tmk, tmv;
-  int rc = make_kv_map(pl, k_cache, &tmk);
-  if (rc == DA_OK) rc = make_kv_map(pl, v_cache, &tmv);
+  int rc = make_kv_map(pl, k_cache, mma, &tmk);
+  if (rc == DA_OK) rc = make_kv_map(pl, v_cache, mma, &tmv);
   if (rc != DA_OK) return rc;
 
   Params kp;
@@ -545,7 +575,13 @@ int decode_attn_run_ex(const da_plan* plan, const da_run_args* args) {
         pl.num_sms, (long long)pl.n_groups * pl.recompute_splits));
     rcfg.attrs = pdl;
     rcfg.numAttrs = 1;
-    void* rargs[3] = {&rp, &tmk, &tmv};
+    CUtensorMap rk = tmk, rv = tmv;   // the recompute runs CUDA-core consumers: plain tiles
+    if (mma) {
+      rc = make_kv_map(pl, k_cache, false, &rk);
+      if (rc == DA_OK) rc = make_kv_map(pl, v_cache, false, &rv);
+      if (rc != DA_OK) return rc;
+    }
+    void* rargs[3] = {&rp, &rk, &rv};
     e = cudaLaunchKernelExC(&rcfg, rfn, rargs);
     if (e != cudaSuccess) return cuda_fail(e, "launching the recompute kernel");
   }

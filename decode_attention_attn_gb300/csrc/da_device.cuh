@@ -12,8 +12,14 @@
 namespace da {
 
 // ---- fixed kernel geometry ------------------------------------------------------------
-constexpr int kConsumerWarps = 8;                       // compute warps per CTA
-constexpr int kThreads = (kConsumerWarps + 1) * 32;     // + one TMA producer warp
+constexpr int kConsumerWarps = 8;                       // compute warps per CTA (2 warpgroups)
+constexpr int kThreads = (kConsumerWarps + 4) * 32;     // + a producer warpgroup (1 working warp)
+constexpr int kLaunchRegs = 168;                        // 65536 / 384, rounded to 8
+constexpr int kConsumerRegs = 216;                      // after setmaxnreg.inc
+constexpr int kProducerRegs = 72;                       // after setmaxnreg.dec
+static_assert(kConsumerWarps * 32 * kConsumerRegs + 4 * 32 * kProducerRegs <=
+                  (kConsumerWarps + 4) * 32 * kLaunchRegs,
+              "the register split must fit the launch allocation");
 constexpr int kTokensPerWarp = 8;                       // KV rows a consumer warp takes per stage
 constexpr int kStageTokens = kConsumerWarps * kTokensPerWarp;   // 64 KV rows per stage
 constexpr int kMaxStages = 8;
@@ -85,11 +91,41 @@ struct MergeParams {
 // ---- shared-memory layout (host and device compute it identically) ------------------------
 struct Layout {
   uint32_t stage_bytes, k_off, v_off, q_off;
-  uint32_t bar_off, pbuf_off, mm_off, ml_off, mflag_off, macc_off, lens_off, prefix_off, misc_off;
+  uint32_t bar_off, wbuf_off, mm_off, ml_off, mflag_off, lens_off, prefix_off, misc_off;
   uint32_t total;
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+// Split kernels whose unified-max consumers run on the tensor cores (see da_mma.cuh): bf16
+// caches, packed groups of 4 or 8 query heads. Their K/V tiles are TMA-loaded with the 128-byte
+// swizzle (4-D view: 64-element rows, d / 64 of them per token, heads, tokens).
+__host__ __device__ constexpr bool uses_mma(int es, bool is_bf16, int G, bool unified) {
+  return unified && es == 2 && is_bf16 && (G == 4 || G == 8);
+}
+
+// Geometry of a consumer warp's logit transpose: a KV row of D elements of es bytes is split
+// over lg_lanes lanes (16 bytes each); a warp has 32 / lg_lanes lane groups of 8 / that many
+// rows, so each lane group produces v = G * rows partial-sum rows to transpose.
+__host__ __device__ constexpr int tp_lanes(int D, int es) { return D / (16 / es); }
+__host__ __device__ constexpr int tp_values(int D, int G, int es) {
+  return G * (kTokensPerWarp / (32 / tp_lanes(D, es)));
+}
+__host__ __device__ constexpr int tp_row_stride(int D, int es) { return tp_lanes(D, es) + 4; }
+// One lane group's block: v rows of row_stride floats, rounded to 32 floats, plus lg_lanes so
+// that the groups' rows fall on different banks.
+__host__ __device__ constexpr int tp_group_floats(int D, int G, int es) {
+  return (tp_values(D, G, es) * tp_row_stride(D, es) + 31) / 32 * 32 + tp_lanes(D, es);
+}
+// Per-warp scratch (floats): the transpose, the (p, p) pairs and, at a piece's end, the
+// warp's accumulators share it (they are never live at the same time).
+__host__ __device__ constexpr int warp_scratch_floats(int D, int G, int es) {
+  const int tp = (32 / tp_lanes(D, es)) * tp_group_floats(D, G, es);
+  const int pairs = 2 * 2 * kTokensPerWarp * G;   // (p, p) pairs of two batches
+  const int acc = G * D;
+  const int m = tp > pairs ? (tp > acc ? tp : acc) : (pairs > acc ? pairs : acc);
+  return (m + 3) / 4 * 4;
+}
 
 __host__ __device__ inline Layout make_layout(int D, int G, int es, int stages, int batch_smem) {
   Layout L;
@@ -97,13 +133,13 @@ __host__ __device__ inline Layout make_layout(int D, int G, int es, int stages, 
   L.k_off = 0;
   L.v_off = kv;
   L.q_off = 2 * kv;
-  L.stage_bytes = align_up(2 * kv + (uint32_t)G * D * es, 128);
+  L.stage_bytes = align_up(2 * kv + (uint32_t)G * D * es, 1024);   // swizzled tiles: 1 KB
   uint32_t off = (uint32_t)stages * L.stage_bytes;
   L.bar_off = off;
   off += 2u * stages * 8u;
   off = align_up(off, 16);
-  L.pbuf_off = off;
-  off += (uint32_t)kConsumerWarps * kTokensPerWarp * G * 8u;   // (p, p) pairs
+  L.wbuf_off = off;
+  off += (uint32_t)kConsumerWarps * warp_scratch_floats(D, G, es) * 4u;
   L.mm_off = off;
   off += (uint32_t)kConsumerWarps * G * 4u;
   L.ml_off = off;
@@ -111,8 +147,6 @@ __host__ __device__ inline Layout make_layout(int D, int G, int es, int stages, 
   L.mflag_off = off;
   off += (uint32_t)kConsumerWarps * 4u;
   off = align_up(off, 16);
-  L.macc_off = off;
-  off += (uint32_t)kConsumerWarps * G * D * 4u;
   L.lens_off = off;
   off += (uint32_t)batch_smem * 4u;
   L.prefix_off = off;
@@ -120,7 +154,7 @@ __host__ __device__ inline Layout make_layout(int D, int G, int es, int stages, 
   off = align_up(off, 16);
   L.misc_off = off;
   off += 16;
-  L.total = off + 128;   // slack for aligning the dynamic smem base to 128 bytes
+  L.total = off + 1024;   // slack for aligning the dynamic smem base to 1024 bytes
   return L;
 }
 
@@ -200,6 +234,17 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// 4-D tiled TMA load (the swizzled [tokens, heads, d / 64, 64] view of a cache).
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y, int z, int w, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar)),
+      "l"(policy)
+      : "memory");
+}
+
 // Contiguous bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
                                           uint64_t* bar) {
@@ -232,14 +277,31 @@ __device__ __forceinline__ float fast_log2(float x) {
   return y;
 }
 
-// Two FP32 fused multiply-adds in one instruction: (d.x, d.y) = (a.x * b.x + d.x, a.y * b.y + d.y)
-__device__ __forceinline__ void ffma2(float2& d, const float2 a, const float2 b) {
-  unsigned long long dd, aa, bb;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(aa) : "f"(a.x), "f"(a.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(bb) : "f"(b.x), "f"(b.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(dd) : "f"(d.x), "f"(d.y));
-  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(dd) : "l"(aa), "l"(bb));
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(dd));
+// Two FP32 values held in one 64-bit register pair, operated on by the packed FP32
+// instructions (fma/mul/add .f32x2). Keeping operands in this form end to end lets every
+// packed instruction take its registers directly, with no packing moves.
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 f2_pack(float a, float b) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ f32x2 f2_pack_bits(uint32_t a, uint32_t b) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(f32x2 v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ void f2_fma(f32x2& d, f32x2 a, f32x2 b) {   // d = a * b + d
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+__device__ __forceinline__ f32x2 f2_mul(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
 }
 
 // ---- element conversion of one 16-byte chunk to FP32 ------------------------------------
@@ -249,6 +311,10 @@ struct Elem;
 template <>
 struct Elem<float> {
   static constexpr int kPerChunk = 4;
+  __device__ __forceinline__ static void to_pairs(const uint4 c, f32x2* f) {
+    f[0] = f2_pack_bits(c.x, c.y);
+    f[1] = f2_pack_bits(c.z, c.w);
+  }
   __device__ __forceinline__ static void to_f32(const uint4 c, float* f) {
     f[0] = __uint_as_float(c.x);
     f[1] = __uint_as_float(c.y);
@@ -260,6 +326,11 @@ struct Elem<float> {
 template <>
 struct Elem<__nv_bfloat16> {
   static constexpr int kPerChunk = 8;
+  __device__ __forceinline__ static void to_pairs(const uint4 c, f32x2* f) {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f[i] = f2_pack_bits(w[i] << 16, w[i] & 0xffff0000u);
+  }
   // bfloat16 is the upper half of a binary32: widening is a shift / mask.
   __device__ __forceinline__ static void to_f32(const uint4 c, float* f) {
     const uint32_t w[4] = {c.x, c.y, c.z, c.w};
@@ -274,6 +345,16 @@ struct Elem<__nv_bfloat16> {
 template <>
 struct Elem<__half> {
   static constexpr int kPerChunk = 8;
+  __device__ __forceinline__ static void to_pairs(const uint4 c, f32x2* f) {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __half2 h;
+      memcpy(&h, &w[i], 4);
+      const float2 v = __half22float2(h);
+      f[i] = f2_pack(v.x, v.y);
+    }
+  }
   __device__ __forceinline__ static void to_f32(const uint4 c, float* f) {
     const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll

@@ -33,7 +33,10 @@
 // are converted back to natural log on output.
 #pragma once
 
+#include <type_traits>
+
 #include "da_device.cuh"
+#include "da_mma.cuh"
 
 namespace da {
 
@@ -161,7 +164,7 @@ __device__ __forceinline__ bool sched_next(Sched& s, const Params& p, Piece& pc)
 }
 
 // ---- producer warp -------------------------------------------------------------------
-template <typename T, int D, int G>
+template <typename T, int D, int G, bool SWZ>
 __device__ __forceinline__ void run_producer(const Params& p, Sched s, uint8_t* stages,
                                              const Layout& L, uint64_t* full, uint64_t* empty,
                                              const CUtensorMap* tmk, const CUtensorMap* tmv,
@@ -226,10 +229,17 @@ __device__ __forceinline__ void run_producer(const Params& p, Sched s, uint8_t* 
 #pragma unroll
           for (int bi = 0; bi < kStageTokens / 8; ++bi) {
             if (bi < nbox) {
-              tma_load_3d(st + L.k_off + bi * box * C::kRowBytes, tmk, &full[slot], 0, pc.kvh,
-                          zs[bi], pol);
-              tma_load_3d(st + L.v_off + bi * box * C::kRowBytes, tmv, &full[slot], 0, pc.kvh,
-                          zs[bi], pol);
+              if constexpr (SWZ) {
+                tma_load_4d(st + L.k_off + bi * box * C::kRowBytes, tmk, &full[slot], 0, 0,
+                            pc.kvh, zs[bi], pol);
+                tma_load_4d(st + L.v_off + bi * box * C::kRowBytes, tmv, &full[slot], 0, 0,
+                            pc.kvh, zs[bi], pol);
+              } else {
+                tma_load_3d(st + L.k_off + bi * box * C::kRowBytes, tmk, &full[slot], 0, pc.kvh,
+                            zs[bi], pol);
+                tma_load_3d(st + L.v_off + bi * box * C::kRowBytes, tmv, &full[slot], 0, pc.kvh,
+                            zs[bi], pol);
+              }
             }
           }
         }
@@ -239,8 +249,13 @@ __device__ __forceinline__ void run_producer(const Params& p, Sched s, uint8_t* 
         const int z = pc.b * p.max_seq_len + ts;
         mbar_arrive_expect_tx(&full[slot], bytes);
         if (j == 0) bulk_load(st + L.q_off, qsrc, C::kQBytes, &full[slot]);
-        tma_load_3d(st + L.k_off, tmk, &full[slot], 0, pc.kvh, z, pol);
-        tma_load_3d(st + L.v_off, tmv, &full[slot], 0, pc.kvh, z, pol);
+        if constexpr (SWZ) {
+          tma_load_4d(st + L.k_off, tmk, &full[slot], 0, 0, pc.kvh, z, pol);
+          tma_load_4d(st + L.v_off, tmv, &full[slot], 0, 0, pc.kvh, z, pol);
+        } else {
+          tma_load_3d(st + L.k_off, tmk, &full[slot], 0, pc.kvh, z, pol);
+          tma_load_3d(st + L.v_off, tmv, &full[slot], 0, pc.kvh, z, pol);
+        }
       }
       __syncwarp();
     }
@@ -275,64 +290,110 @@ struct LaneMap {
   __device__ __forceinline__ int idx(int i) const { return j[i] * G + g[i]; }
 };
 
-// One stage: the warp's 8 rows. p values are published to shared memory as (p, p) pairs so
-// that P . V takes its packed-FMA operands straight from a 16-byte load.
+// Two consecutive stages at once: the warp's 8 rows of each are two independent batches whose
+// q . k and P . V chains interleave (when there is no second stage, n[1] == 0 masks every row
+// of the second batch, which then reads stale but in-bounds shared memory). p values are
+// published to shared memory as (p, p) pairs so that P . V takes its packed-FMA operands
+// straight from a 16-byte load.
 template <typename T, int D, int G, bool UNIFIED>
-__device__ __forceinline__ void consume_stage(const Params& p, const LaneMap<T, D, G>& lm,
-                                              const uint8_t* ks, const uint8_t* vs, int n,
-                                              const float (&q)[G][Cfg<T, D, G>::kEpl],
-                                              float (&acc)[G][Cfg<T, D, G>::kEpl],
-                                              float (&dl)[Cfg<T, D, G>::kNv], float (&m)[G],
-                                              uint32_t& fmask, float2* pwarp) {
+__device__ __forceinline__ void consume_stages(const Params& p, const LaneMap<T, D, G>& lm,
+                                               const uint8_t* const (&ks)[2],
+                                               const uint8_t* const (&vs)[2], const int (&n)[2],
+                                               const f32x2 (&q2)[G][Cfg<T, D, G>::kEpl / 2],
+                                               f32x2 (&acc2)[G][Cfg<T, D, G>::kEpl / 2],
+                                               float (&dl)[Cfg<T, D, G>::kNv], float (&m)[G],
+                                               uint32_t& fmask, float* wscr) {
   using C = Cfg<T, D, G>;
-  constexpr int E = C::kEpl;
-  float2* pw = pwarp + lm.lg * C::kV;
+  constexpr int E2 = C::kEpl / 2;
+  constexpr int RS = tp_row_stride(D, C::kEs);
+  constexpr int NB = 2;   // an absent second stage has n[1] == 0: all its rows are masked
 
   // q . k for the lane group's rows and all G heads: partial sums over this lane's chunk
-  float part[C::kV];
+  float part[NB][C::kV];
 #pragma unroll
-  for (int j = 0; j < C::kT; ++j) {
-    const uint4 c =
-        *reinterpret_cast<const uint4*>(ks + (lm.row0 + j) * C::kRowBytes + lm.li * 16);
-    float kf[E];
-    Elem<T>::to_f32(c, kf);
+  for (int b = 0; b < NB; ++b) {
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float2 s2 = make_float2(0.f, 0.f);
+    for (int j = 0; j < C::kT; ++j) {
+      const uint4 c =
+          *reinterpret_cast<const uint4*>(ks[b] + (lm.row0 + j) * C::kRowBytes + lm.li * 16);
+      f32x2 kp[E2];
+      Elem<T>::to_pairs(c, kp);
 #pragma unroll
-      for (int e = 0; e < E; e += 2)
-        ffma2(s2, make_float2(q[g][e], q[g][e + 1]), make_float2(kf[e], kf[e + 1]));
-      part[j * G + g] = s2.x + s2.y;
+      for (int g = 0; g < G; ++g) {
+        f32x2 s2 = f2_mul(q2[g][0], kp[0]);
+#pragma unroll
+        for (int e = 1; e < E2; ++e) f2_fma(s2, q2[g][e], kp[e]);
+        float lo, hi;
+        f2_unpack(s2, lo, hi);
+        part[b][j * G + g] = lo + hi;
+      }
     }
   }
-  Reduce<C::kV, C::kLg / 2>::run(part, lm.li);
-
-  bool valid[C::kNv];
+  // Transpose-reduce through shared memory: lane li of the group stores its kV partial sums
+  // as column li of a [kV][kLg] block (rows padded so that every 16-byte read of a row hits
+  // its own banks), then each lane sums the kLg partials of its logit's row.
+  float* tb = wscr + lm.lg * tp_group_floats(D, G, C::kEs);
+  float sc[NB][C::kNv];
 #pragma unroll
-  for (int i = 0; i < C::kNv; ++i) valid[i] = lm.row0 + lm.j[i] < n;
+  for (int b = 0; b < NB; ++b) {
+#pragma unroll
+    for (int v = 0; v < C::kV; ++v) tb[v * RS + lm.li] = part[b][v];
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < C::kNv; ++i) {
+      const float4* row = reinterpret_cast<const float4*>(tb + lm.idx(i) * RS);
+      float4 acc4 = row[0];
+#pragma unroll
+      for (int c = 1; c < C::kLg / 4; ++c) {
+        const float4 x = row[c];
+        acc4.x += x.x;
+        acc4.y += x.y;
+        acc4.z += x.z;
+        acc4.w += x.w;
+      }
+      sc[b][i] = (acc4.x + acc4.y) + (acc4.z + acc4.w);
+    }
+    __syncwarp();   // the block is reused by the next batch and for p below
+  }
+
+  // p pairs: batch b at pwarp + b * 8 * G, lane group lg at + lg * kV
+  float2* pwarp = reinterpret_cast<float2*>(wscr);
+  bool valid[NB][C::kNv];
+#pragma unroll
+  for (int b = 0; b < NB; ++b)
+#pragma unroll
+    for (int i = 0; i < C::kNv; ++i) valid[b][i] = lm.row0 + lm.j[i] < n[b];
 
   if constexpr (UNIFIED) {
 #pragma unroll
-    for (int i = 0; i < C::kNv; ++i) {
-      const float s = part[i];
-      const float pr = valid[i] ? fast_exp2(s - p.phi2) : 0.f;
-      if (valid[i] && (s < p.lo2 || s > p.hi2)) fmask |= 1u << lm.g[i];
-      dl[i] += pr;
-      if (lm.writer) pw[lm.idx(i)] = make_float2(pr, pr);
+    for (int b = 0; b < NB; ++b) {
+        float2* pw = pwarp + b * kTokensPerWarp * G + lm.lg * C::kV;
+#pragma unroll
+      for (int i = 0; i < C::kNv; ++i) {
+        const float s = sc[b][i];
+        const float pr = valid[b][i] ? fast_exp2(s - p.phi2) : 0.f;
+        if (valid[b][i] && (s < p.lo2 || s > p.hi2)) fmask |= 1u << lm.g[i];
+        dl[i] += pr;
+        if (lm.writer) pw[lm.idx(i)] = make_float2(pr, pr);
+      }
     }
   } else {
 #pragma unroll
-    for (int i = 0; i < C::kNv; ++i) {
-      const float s = valid[i] ? part[i] : -INFINITY;
-      if (lm.writer) pw[lm.idx(i)] = make_float2(s, s);
+    for (int b = 0; b < NB; ++b) {
+      float2* pw = pwarp + b * kTokensPerWarp * G + lm.lg * C::kV;
+#pragma unroll
+      for (int i = 0; i < C::kNv; ++i) {
+        const float s = valid[b][i] ? sc[b][i] : -INFINITY;
+        if (lm.writer) pw[lm.idx(i)] = make_float2(s, s);
+      }
     }
     __syncwarp();
-    // per-head maximum over the warp's 8 rows of this stage, then the online update
+    // per-head maximum over the warp's rows of both stages, then one online update
     float tm[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) tm[g] = -INFINITY;
 #pragma unroll
-    for (int r = 0; r < kTokensPerWarp; ++r)
+    for (int r = 0; r < NB * kTokensPerWarp; ++r)
 #pragma unroll
       for (int g = 0; g < G; ++g) tm[g] = fmaxf(tm[g], pwarp[r * G + g].x);
     float alpha[G];
@@ -341,8 +402,9 @@ __device__ __forceinline__ void consume_stage(const Params& p, const LaneMap<T, 
       const float mn = fmaxf(m[g], tm[g]);
       alpha[g] = mn == -INFINITY ? 1.f : fast_exp2(m[g] - mn);
       m[g] = mn;
+      const f32x2 a2 = f2_pack(alpha[g], alpha[g]);
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[g][e] *= alpha[g];
+      for (int e = 0; e < E2; ++e) acc2[g][e] = f2_mul(acc2[g][e], a2);
     }
     __syncwarp();
 #pragma unroll
@@ -354,41 +416,45 @@ __device__ __forceinline__ void consume_stage(const Params& p, const LaneMap<T, 
           mg = m[g];
           ag = alpha[g];
         }
-      const float pr = valid[i] ? fast_exp2(part[i] - mg) : 0.f;
-      dl[i] = dl[i] * ag + pr;
-      if (lm.writer) pw[lm.idx(i)] = make_float2(pr, pr);
+      dl[i] *= ag;
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        const float pr = valid[b][i] ? fast_exp2(sc[b][i] - mg) : 0.f;
+        dl[i] += pr;
+        float2* pw = pwarp + b * kTokensPerWarp * G + lm.lg * C::kV;
+        if (lm.writer) pw[lm.idx(i)] = make_float2(pr, pr);
+      }
     }
   }
   __syncwarp();
 
   // P . V: every lane of the group accumulates its chunk of d for all heads
 #pragma unroll
-  for (int j = 0; j < C::kT; ++j) {
-    if (lm.row0 + j < n) {
-      const uint4 c =
-          *reinterpret_cast<const uint4*>(vs + (lm.row0 + j) * C::kRowBytes + lm.li * 16);
-      float vf[E];
-      Elem<T>::to_f32(c, vf);
-      float2 pp[G];
-      if constexpr (G == 1) {
-        pp[0] = pw[j];
-      } else {
+  for (int b = 0; b < NB; ++b) {
+    const float2* pw = pwarp + b * kTokensPerWarp * G + lm.lg * C::kV;
 #pragma unroll
-        for (int g = 0; g < G; g += 2) {
-          const float4 two = *reinterpret_cast<const float4*>(pw + j * G + g);
-          pp[g] = make_float2(two.x, two.y);
-          pp[g + 1] = make_float2(two.z, two.w);
+    for (int j = 0; j < C::kT; ++j) {
+      if (lm.row0 + j < n[b]) {
+        const uint4 c =
+            *reinterpret_cast<const uint4*>(vs[b] + (lm.row0 + j) * C::kRowBytes + lm.li * 16);
+        f32x2 vp[E2];
+        Elem<T>::to_pairs(c, vp);
+        f32x2 pp[G];
+        const f32x2* pwj = reinterpret_cast<const f32x2*>(pw + j * G);
+        if constexpr (G == 1) {
+          pp[0] = pwj[0];
+        } else {
+#pragma unroll
+          for (int g = 0; g < G; g += 2) {
+            const ulonglong2 two2 = *reinterpret_cast<const ulonglong2*>(pwj + g);
+            pp[g] = two2.x;
+            pp[g + 1] = two2.y;
+          }
         }
-      }
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
+        for (int g = 0; g < G; ++g)
 #pragma unroll
-        for (int e = 0; e < E; e += 2) {
-          float2 a2 = make_float2(acc[g][e], acc[g][e + 1]);
-          ffma2(a2, pp[g], make_float2(vf[e], vf[e + 1]));
-          acc[g][e] = a2.x;
-          acc[g][e + 1] = a2.y;
-        }
+          for (int e = 0; e < E2; ++e) f2_fma(acc2[g][e], pp[g], vp[e]);
       }
     }
   }
@@ -396,19 +462,18 @@ __device__ __forceinline__ void consume_stage(const Params& p, const LaneMap<T, 
 }
 
 // ---- consumer warps: end of a piece ---------------------------------------------------
-template <typename T, int D, int G, bool UNIFIED>
-__device__ __forceinline__ void finish_piece(const Params& p, const Piece& pc,
-                                             const LaneMap<T, D, G>& lm,
+// Publish a CUDA-core warp's piece state to the shared scratch: m, l per head and the
+// accumulators as [warp][G][D].
+template <typename T, int D, int G>
+__device__ __forceinline__ void publish_cuda(const LaneMap<T, D, G>& lm,
                                              float (&acc)[G][Cfg<T, D, G>::kEpl],
                                              const float (&dl)[Cfg<T, D, G>::kNv],
                                              const float (&m)[G], uint32_t fmask, float* mm,
-                                             float* ml, uint32_t* mflag, float* macc, int* misc,
-                                             int warp, int lane, int ctid) {
+                                             float* ml, uint32_t* mflag, float* wbuf, int warp,
+                                             int lane) {
   using C = Cfg<T, D, G>;
   constexpr int E = C::kEpl;
-  constexpr int kCT = kConsumerWarps * 32;
-  constexpr float kLn2 = 0.6931471805599453f;
-
+  constexpr int W = warp_scratch_floats(D, G, C::kEs);
   // the warp's denominators: each head's p values are spread over the lanes holding it
   float den[G];
 #pragma unroll
@@ -433,7 +498,7 @@ __device__ __forceinline__ void finish_piece(const Params& p, const Piece& pc,
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
-      for (int e = 0; e < E; ++e) macc[(warp * G + g) * D + lm.li * E + e] = acc[g][e];
+      for (int e = 0; e < E; ++e) wbuf[warp * W + g * D + lm.li * E + e] = acc[g][e];
   }
   if (lane == 0) {
 #pragma unroll
@@ -443,6 +508,42 @@ __device__ __forceinline__ void finish_piece(const Params& p, const Piece& pc,
     }
     mflag[warp] = fm;
   }
+}
+
+// Publish a tensor-core warp's piece state (same scratch format as publish_cuda).
+template <typename T, int D, int G>
+__device__ __forceinline__ void publish_mma(const MmaState<D, G>& st, float phi2, uint32_t fmask,
+                                            float* mm, float* ml, uint32_t* mflag, float* wbuf,
+                                            int warp, int lane) {
+  constexpr int W = warp_scratch_floats(D, G, (int)sizeof(T));
+  const int head = lane >> 2, c0 = 2 * (lane & 3);
+  float den = st.den;
+  den += __shfl_xor_sync(0xffffffffu, den, 1);
+  den += __shfl_xor_sync(0xffffffffu, den, 2);
+  const uint32_t fm = __reduce_or_sync(0xffffffffu, fmask);
+  if (head < G) {
+#pragma unroll
+    for (int j = 0; j < D / 8; ++j) {
+      wbuf[warp * W + head * D + 8 * j + c0] = st.o[j][0];
+      wbuf[warp * W + head * D + 8 * j + c0 + 1] = st.o[j][1];
+    }
+    if ((lane & 3) == 0) {
+      mm[warp * G + head] = phi2;
+      ml[warp * G + head] = den;
+    }
+  }
+  if (lane == 0) mflag[warp] = fm;
+}
+
+// The 8 consumer warps' published states -> one partial (or the output, when the piece is
+// its group's only one); the recompute pass merges its own pieces here.
+template <typename T, int D, int G>
+__device__ __forceinline__ void combine_piece(const Params& p, const Piece& pc, float* mm,
+                                              float* ml, uint32_t* mflag, float* wbuf, int* misc,
+                                              int warp, int lane, int ctid) {
+  constexpr int kCT = kConsumerWarps * 32;
+  constexpr float kLn2 = 0.6931471805599453f;
+  constexpr int W = warp_scratch_floats(D, G, (int)sizeof(T));
   named_bar_sync(1, kCT);
 
   uint32_t fl = 0;
@@ -465,7 +566,7 @@ __device__ __forceinline__ void finish_piece(const Params& p, const Piece& pc,
       if (l > 0.f) {
         const float f = fast_exp2(mm[w * G + g] - M);
         sum += f * l;
-        num += f * macc[(w * G + g) * D + d];
+        num += f * wbuf[w * W + g * D + d];
       }
     }
     const float o = sum > 0.f ? num / sum : 0.f;
@@ -510,7 +611,7 @@ __device__ __forceinline__ void finish_piece(const Params& p, const Piece& pc,
       // parallel over slots so the merge pays the L2 latency a few times, not per slot.
       __threadfence();
       const int S = pc.nslots;
-      float* wts = macc;              // [S, G] weights (scratch reused; S <= 8 * D)
+      float* wts = wbuf;              // [S, G] weights (scratch reused; S <= 8 * D)
       float* hsum = mm;               // [G] sum of weights
       float* hmax = ml;               // [G] maximum partial LSE
       const float* pl = p.part_l + (long long)pc.slot_base * G;
@@ -585,57 +686,138 @@ __device__ __forceinline__ void run_consumers(const Params& p, Sched s, uint8_t*
   using C = Cfg<T, D, G>;
   constexpr int E = C::kEpl;
   const uint32_t NS = (uint32_t)p.stages;
-  float2* pwarp = reinterpret_cast<float2*>(smem + L.pbuf_off) + warp * kTokensPerWarp * G;
+  float* wbuf = reinterpret_cast<float*>(smem + L.wbuf_off);
+  float* wscr = wbuf + warp * warp_scratch_floats(D, G, C::kEs);
   float* mm = reinterpret_cast<float*>(smem + L.mm_off);
   float* ml = reinterpret_cast<float*>(smem + L.ml_off);
   uint32_t* mflag = reinterpret_cast<uint32_t*>(smem + L.mflag_off);
-  float* macc = reinterpret_cast<float*>(smem + L.macc_off);
   int* misc = reinterpret_cast<int*>(smem + L.misc_off);
   const LaneMap<T, D, G> lm(warp, lane);
   const int ctid = warp * 32 + lane;
   uint32_t k = 0;
   bool dead = false;
   Piece pc;
+  constexpr int E2 = E / 2;
   while (sched_next(s, p, pc)) {
-    float acc[G][E], dl[C::kNv], m[G], q[G][E];
+    float dl[C::kNv], m[G];
+    f32x2 acc2[G][E2], q2[G][E2];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       m[g] = UNIFIED ? p.phi2 : -INFINITY;
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        acc[g][e] = 0.f;
-        q[g][e] = 0.f;
+      for (int e = 0; e < E2; ++e) {
+        acc2[g][e] = 0ull;   // +0.0f in both halves
+        q2[g][e] = 0ull;
       }
     }
 #pragma unroll
     for (int i = 0; i < C::kNv; ++i) dl[i] = 0.f;
     uint32_t fmask = 0;
-    for (int ts = pc.t0, j = 0; ts < pc.t1; ts += kStageTokens, ++j, ++k) {
-      const uint32_t slot = k % NS, ph = (k / NS) & 1u;
-      if (!dead && !mbar_wait(&full[slot], ph)) {
+    const int nst = (pc.t1 - pc.t0 + kStageTokens - 1) / kStageTokens;
+    for (int j = 0; j < nst; j += 2) {
+      const bool pair = j + 1 < nst;
+      const uint32_t s0 = k % NS, s1 = (k + 1) % NS;
+      if (!dead && !mbar_wait(&full[s0], (k / NS) & 1u)) {
         dead = true;
         if (lane == 0) atomicOr(p.status, kStatusTimeout);
       }
-      const uint8_t* st = stages + slot * L.stage_bytes;
+      if (pair && !dead && !mbar_wait(&full[s1], ((k + 1) / NS) & 1u)) {
+        dead = true;
+        if (lane == 0) atomicOr(p.status, kStatusTimeout);
+      }
+      const uint8_t* st0 = stages + s0 * L.stage_bytes;
+      const uint8_t* st1 = stages + s1 * L.stage_bytes;
       if (j == 0) {
+        const f32x2 qs = f2_pack(p.qscale, p.qscale);
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           const uint4 c =
-              *reinterpret_cast<const uint4*>(st + L.q_off + g * C::kRowBytes + lm.li * 16);
-          Elem<T>::to_f32(c, q[g]);
+              *reinterpret_cast<const uint4*>(st0 + L.q_off + g * C::kRowBytes + lm.li * 16);
+          Elem<T>::to_pairs(c, q2[g]);
 #pragma unroll
-          for (int e = 0; e < E; ++e) q[g][e] *= p.qscale;
+          for (int e = 0; e < E2; ++e) q2[g][e] = f2_mul(q2[g][e], qs);
         }
       }
+      const int ts = pc.t0 + j * kStageTokens;
+      const int n[2] = {min(kStageTokens, pc.t1 - ts),
+                        pair ? min(kStageTokens, pc.t1 - ts - kStageTokens) : 0};
+      const uint8_t* const kss[2] = {st0 + L.k_off, st1 + L.k_off};
+      const uint8_t* const vss[2] = {st0 + L.v_off, st1 + L.v_off};
       if (!dead)
-        consume_stage<T, D, G, UNIFIED>(p, lm, st + L.k_off, st + L.v_off,
-                                        min(kStageTokens, pc.t1 - ts), q, acc, dl, m, fmask,
-                                        pwarp);
+        consume_stages<T, D, G, UNIFIED>(p, lm, kss, vss, n, q2, acc2, dl, m, fmask, wscr);
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[slot]);
+      if (lane == 0) {
+        mbar_arrive(&empty[s0]);
+        if (pair) mbar_arrive(&empty[s1]);
+      }
+      k += pair ? 2u : 1u;
     }
-    finish_piece<T, D, G, UNIFIED>(p, pc, lm, acc, dl, m, fmask, mm, ml, mflag, macc, misc,
-                                   warp, lane, ctid);
+    float acc[G][E];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int e = 0; e < E2; ++e) f2_unpack(acc2[g][e], acc[g][2 * e], acc[g][2 * e + 1]);
+    publish_cuda<T, D, G>(lm, acc, dl, m, fmask, mm, ml, mflag, wbuf, warp, lane);
+    combine_piece<T, D, G>(p, pc, mm, ml, mflag, wbuf, misc, warp, lane, ctid);
+  }
+}
+
+// Tensor-core consumers (unified softmax, bf16, G >= 4): same stage-pair loop as
+// run_consumers, the math in mma_consume.
+template <typename T, int D, int G>
+__device__ __forceinline__ void run_consumers_mma(const Params& p, Sched s, uint8_t* stages,
+                                                  const Layout& L, uint64_t* full,
+                                                  uint64_t* empty, uint8_t* smem, int warp,
+                                                  int lane) {
+  const uint32_t NS = (uint32_t)p.stages;
+  float* wbuf = reinterpret_cast<float*>(smem + L.wbuf_off);
+  float* mm = reinterpret_cast<float*>(smem + L.mm_off);
+  float* ml = reinterpret_cast<float*>(smem + L.ml_off);
+  uint32_t* mflag = reinterpret_cast<uint32_t*>(smem + L.mflag_off);
+  int* misc = reinterpret_cast<int*>(smem + L.misc_off);
+  const int ctid = warp * 32 + lane;
+  const int row0 = warp * kTokensPerWarp;
+  uint32_t k = 0;
+  bool dead = false;
+  Piece pc;
+  while (sched_next(s, p, pc)) {
+    MmaState<D, G> st;
+#pragma unroll
+    for (int j = 0; j < D / 8; ++j)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) st.o[j][i] = 0.f;
+    st.den = 0.f;
+    uint32_t fmask = 0;
+    const int nst = (pc.t1 - pc.t0 + kStageTokens - 1) / kStageTokens;
+    for (int j = 0; j < nst; j += 2) {
+      const bool pair = j + 1 < nst;
+      const uint32_t s0 = k % NS, s1 = (k + 1) % NS;
+      if (!dead && !mbar_wait(&full[s0], (k / NS) & 1u)) {
+        dead = true;
+        if (lane == 0) atomicOr(p.status, kStatusTimeout);
+      }
+      if (pair && !dead && !mbar_wait(&full[s1], ((k + 1) / NS) & 1u)) {
+        dead = true;
+        if (lane == 0) atomicOr(p.status, kStatusTimeout);
+      }
+      const uint8_t* st0 = stages + s0 * L.stage_bytes;
+      const uint8_t* st1 = stages + s1 * L.stage_bytes;
+      if (j == 0) mma_load_q<D, G>(st, st0 + L.q_off, lane);
+      const int ts = pc.t0 + j * kStageTokens;
+      const int n[2] = {min(kStageTokens, pc.t1 - ts),
+                        pair ? min(kStageTokens, pc.t1 - ts - kStageTokens) : 0};
+      const uint8_t* const kss[2] = {st0 + L.k_off, st1 + L.k_off};
+      const uint8_t* const vss[2] = {st0 + L.v_off, st1 + L.v_off};
+      if (!dead) mma_consume<D, G>(p, st, kss, vss, n, row0, lane, fmask);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&empty[s0]);
+        if (pair) mbar_arrive(&empty[s1]);
+      }
+      k += pair ? 2u : 1u;
+    }
+    publish_mma<T, D, G>(st, p.phi2, fmask, mm, ml, mflag, wbuf, warp, lane);
+    combine_piece<T, D, G>(p, pc, mm, ml, mflag, wbuf, misc, warp, lane, ctid);
   }
 }
 
@@ -645,8 +827,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tmv) {
   using C = Cfg<T, D, G>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
-                                             ~static_cast<uintptr_t>(127));
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
   const Layout L = make_layout(D, G, C::kEs, p.stages, p.batch_smem);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   uint64_t* empty = full + p.stages;
@@ -735,10 +917,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_launch_dependents();
 
   uint8_t* stages = smem;
-  if (warp == kConsumerWarps)
-    run_producer<T, D, G>(p, s, stages, L, full, empty, &tmk, &tmv, lane);
-  else
-    run_consumers<T, D, G, UNIFIED>(p, s, stages, L, full, empty, smem, warp, lane);
+  // Registers move from the producer warpgroup (one working warp) to the two consumer
+  // warpgroups: 8 * 32 * kConsumerRegs + 4 * 32 * kProducerRegs equals the launch's
+  // 12 * 32 * 168 (checked on the host before the first launch).
+  constexpr bool kMma = uses_mma(sizeof(T), std::is_same<T, __nv_bfloat16>::value, G, UNIFIED);
+  if (warp < kConsumerWarps) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
+    if constexpr (kMma)
+      run_consumers_mma<T, D, G>(p, s, stages, L, full, empty, smem, warp, lane);
+    else
+      run_consumers<T, D, G, UNIFIED>(p, s, stages, L, full, empty, smem, warp, lane);
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
+    if (warp == kConsumerWarps)
+      run_producer<T, D, G, kMma>(p, s, stages, L, full, empty, &tmk, &tmv, lane);
+  }
 
   if (p.use_list) {
     // the recompute pass's last CTA resets the flagged list for the next run
