@@ -163,16 +163,20 @@ __device__ __forceinline__ bool sched_next(Sched& s, const Params& p, Piece& pc)
   return true;
 }
 
-// ---- producer warp -------------------------------------------------------------------
+// ---- producer warps ------------------------------------------------------------------
+// Copies are issued by two warps (part 0: K and q, part 1: V) for a contiguous cache and by
+// four for a paged one (parts 2 and 3 take every other page box): one warp's TMA issue rate
+// cannot keep up with a stage made of several small page boxes.
 template <typename T, int D, int G, bool SWZ>
 __device__ __forceinline__ void run_producer(const Params& p, Sched s, uint8_t* stages,
                                              const Layout& L, uint64_t* full, uint64_t* empty,
                                              const CUtensorMap* tmk, const CUtensorMap* tmv,
-                                             int lane) {
+                                             int lane, int part) {
   using C = Cfg<T, D, G>;
   const uint64_t pol = make_evict_first_policy();
   const uint32_t NS = (uint32_t)p.stages;
-  uint32_t k = 0;
+  const int nsub = p.paged ? 2 : 1;   // warps per tensor: K from even parts, V from odd
+  uint32_t k = 0, issued = 0;   // stages passed / one past the last stage with copies
   bool dead = false;
   Piece pc;
   while (sched_next(s, p, pc)) {
@@ -180,7 +184,9 @@ __device__ __forceinline__ void run_producer(const Params& p, Sched s, uint8_t* 
     const int32_t* trow = p.paged ? p.block_table + (long long)pc.b * p.max_blocks : nullptr;
     const char* qsrc = static_cast<const char*>(p.q) +
                        ((long long)pc.b * p.hq + (long long)pc.kvh * G) * D * C::kEs;
-    int wbase = -1, nbase = -1;
+    // Block-table entries of pages [wbase, wbase + 32) (win) and [wbase + 32, wbase + 64)
+    // (wnext), one per lane; wnext is loaded a window ahead of its first use.
+    int wbase = -(1 << 30);
     int32_t win = -1, wnext = -1;
     for (int ts = pc.t0, j = 0; ts < pc.t1; ts += kStageTokens, ++j, ++k) {
       const uint32_t slot = k % NS, ph = (k / NS) & 1u;
@@ -188,82 +194,77 @@ __device__ __forceinline__ void run_producer(const Params& p, Sched s, uint8_t* 
         dead = true;
         if (lane == 0) atomicOr(p.status, kStatusTimeout);
       }
+      dead = __any_sync(0xffffffffu, dead);   // several lanes issue copies: agree on it
+      if (!dead) issued = k + 1;
       const int n = min(kStageTokens, pc.t1 - ts);
       uint8_t* st = stages + slot * L.stage_bytes;
       if (p.paged) {
+        // Lane l of this warp owns box l * nsub + part / 2 of the stage, if there is one (a
+        // stage spans at most 64 / box pages, so every page of it lies in the two windows
+        // once the first one does).
         const int box = p.box_tokens;
         const int nbox = (n + box - 1) / box;
-        int zs[kStageTokens / 8];
-#pragma unroll
-        for (int bi = 0; bi < kStageTokens / 8; ++bi) {
-          if (bi < nbox) {   // warp-uniform
-            const int t = ts + bi * box;
-            const int page = t / p.page_size;
-            const int base = page & ~31;
-            if (base != wbase) {
-              if (base == nbase) {
-                win = wnext;
-              } else {
-                const int idx = base + lane;
-                win = idx < p.max_blocks ? __ldg(trow + idx) : -1;
-              }
-              wbase = base;
-              nbase = base + 32;
-              const int nidx = nbase + lane;
-              wnext = nidx < p.max_blocks ? __ldg(trow + nidx) : -1;   // prefetch next window
-            }
-            const int entry = __shfl_sync(0xffffffffu, win, page & 31);
-            int z = token_row(p, pc.b, t, entry);
-            if (z < 0) {
-              if (lane == 0) atomicOr(p.status, kStatusBadBlockTable);
-              z = p.num_blocks * p.page_size;   // past the pool: the box reads as zeros
-            }
-            zs[bi] = z;
-          }
+        const int first = ts / p.page_size;   // warp-uniform
+        if (first >= wbase + 64 || first < wbase) {
+          wbase = first & ~31;
+          const int i0 = wbase + lane, i1 = wbase + 32 + lane;
+          win = i0 < p.max_blocks ? __ldg(trow + i0) : -1;
+          wnext = i1 < p.max_blocks ? __ldg(trow + i1) : -1;
+        } else if (first >= wbase + 32) {
+          wbase += 32;
+          win = wnext;
+          const int i1 = wbase + 32 + lane;
+          wnext = i1 < p.max_blocks ? __ldg(trow + i1) : -1;
         }
-        if (lane == 0 && !dead) {
+        const int bi = lane * nsub + (part >> 1);   // the box this lane issues, if < nbox
+        const int mine = min(bi, nbox - 1);
+        const int t = ts + mine * box;
+        const int rel = t / p.page_size - wbase;   // 0 <= rel < 64
+        const int e0 = __shfl_sync(0xffffffffu, win, rel & 31);
+        const int e1 = __shfl_sync(0xffffffffu, wnext, rel & 31);
+        int z = token_row(p, pc.b, t, rel < 32 ? e0 : e1);
+        if (z < 0) {
+          if (bi < nbox) atomicOr(p.status, kStatusBadBlockTable);
+          z = p.num_blocks * p.page_size;   // past the pool: the box reads as zeros
+        }
+        if (part == 0 && lane == 0 && !dead) {
           const uint32_t bytes =
               (uint32_t)nbox * box * C::kRowBytes * 2u + (j == 0 ? (uint32_t)C::kQBytes : 0u);
           mbar_arrive_expect_tx(&full[slot], bytes);
           if (j == 0) bulk_load(st + L.q_off, qsrc, C::kQBytes, &full[slot]);
-#pragma unroll
-          for (int bi = 0; bi < kStageTokens / 8; ++bi) {
-            if (bi < nbox) {
-              if constexpr (SWZ) {
-                tma_load_4d(st + L.k_off + bi * box * C::kRowBytes, tmk, &full[slot], 0, 0,
-                            pc.kvh, zs[bi], pol);
-                tma_load_4d(st + L.v_off + bi * box * C::kRowBytes, tmv, &full[slot], 0, 0,
-                            pc.kvh, zs[bi], pol);
-              } else {
-                tma_load_3d(st + L.k_off + bi * box * C::kRowBytes, tmk, &full[slot], 0, pc.kvh,
-                            zs[bi], pol);
-                tma_load_3d(st + L.v_off + bi * box * C::kRowBytes, tmv, &full[slot], 0, pc.kvh,
-                            zs[bi], pol);
-              }
-            }
-          }
+        }
+        __syncwarp();
+        if (bi < nbox && !dead) {
+          const uint32_t off = ((part & 1) == 0 ? L.k_off : L.v_off) + bi * box * C::kRowBytes;
+          const CUtensorMap* tm = (part & 1) == 0 ? tmk : tmv;
+          if constexpr (SWZ)
+            tma_load_4d(st + off, tm, &full[slot], 0, 0, pc.kvh, z, pol);
+          else
+            tma_load_3d(st + off, tm, &full[slot], 0, pc.kvh, z, pol);
         }
       } else if (lane == 0 && !dead) {
-        const uint32_t bytes =
-            (uint32_t)kStageTokens * C::kRowBytes * 2u + (j == 0 ? (uint32_t)C::kQBytes : 0u);
         const int z = pc.b * p.max_seq_len + ts;
-        mbar_arrive_expect_tx(&full[slot], bytes);
-        if (j == 0) bulk_load(st + L.q_off, qsrc, C::kQBytes, &full[slot]);
-        if constexpr (SWZ) {
-          tma_load_4d(st + L.k_off, tmk, &full[slot], 0, 0, pc.kvh, z, pol);
-          tma_load_4d(st + L.v_off, tmv, &full[slot], 0, 0, pc.kvh, z, pol);
-        } else {
-          tma_load_3d(st + L.k_off, tmk, &full[slot], 0, pc.kvh, z, pol);
-          tma_load_3d(st + L.v_off, tmv, &full[slot], 0, pc.kvh, z, pol);
+        if (part == 0) {
+          const uint32_t bytes =
+              (uint32_t)kStageTokens * C::kRowBytes * 2u + (j == 0 ? (uint32_t)C::kQBytes : 0u);
+          mbar_arrive_expect_tx(&full[slot], bytes);
+          if (j == 0) bulk_load(st + L.q_off, qsrc, C::kQBytes, &full[slot]);
         }
+        const uint32_t off = part == 0 ? L.k_off : L.v_off;
+        const CUtensorMap* tm = part == 0 ? tmk : tmv;
+        if constexpr (SWZ)
+          tma_load_4d(st + off, tm, &full[slot], 0, 0, pc.kvh, z, pol);
+        else
+          tma_load_3d(st + off, tm, &full[slot], 0, pc.kvh, z, pol);
       }
       __syncwarp();
     }
   }
-  // Never leave with copies in flight: wait (bounded) for the last issued stages to land.
-  if (!dead && lane == 0) {
-    const uint32_t first = k > NS ? k - NS : 0u;
-    for (uint32_t kk = first; kk < k; ++kk) mbar_wait(&full[kk % NS], (kk / NS) & 1u);
+  // Never leave with copies in flight: wait (bounded) for the last issued stages to land,
+  // after a timeout too.
+  if (lane == 0) {
+    const uint32_t first = issued > NS ? issued - NS : 0u;
+    for (uint32_t kk = first; kk < issued; ++kk) mbar_wait(&full[kk % NS], (kk / NS) & 1u);
   }
 }
 
@@ -929,8 +930,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       run_consumers<T, D, G, UNIFIED>(p, s, stages, L, full, empty, smem, warp, lane);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
-    if (warp == kConsumerWarps)
-      run_producer<T, D, G, kMma>(p, s, stages, L, full, empty, &tmk, &tmv, lane);
+    if (warp < kConsumerWarps + (p.paged ? 4 : 2))
+      run_producer<T, D, G, kMma>(p, s, stages, L, full, empty, &tmk, &tmv, lane,
+                                  warp - kConsumerWarps);
   }
 
   if (p.use_list) {
