@@ -121,6 +121,8 @@ def lib():
         L.decode_attn_run.argtypes = [P, P, P, P, P, P, ctypes.c_float, ctypes.c_int, P, P, P,
                                       P, ctypes.c_size_t, P, ctypes.POINTER(da_stats)]
         L.decode_attn_run_ex.argtypes = [P, ctypes.POINTER(da_run_args)]
+        L.decode_attn_run_static.argtypes = [P, P, P, P, P, P, ctypes.c_float, ctypes.c_int, P,
+                                             P, P, P, ctypes.POINTER(da_stats)]
         L.decode_attn_check_status.argtypes = [P, P, P]
         L.decode_attn_debug_gather.argtypes = [P, P, P, P, P]
         L.decode_attn_destroy.argtypes = [P]
@@ -129,7 +131,8 @@ def lib():
         L.decode_attn_strerror.restype = ctypes.c_char_p
         L.decode_attn_abi_version.argtypes = []
         for name in ("decode_attn_plan", "decode_attn_plan_info", "decode_attn_workspace_init",
-                     "decode_attn_run", "decode_attn_run_ex", "decode_attn_check_status",
+                     "decode_attn_run", "decode_attn_run_ex", "decode_attn_run_static",
+                     "decode_attn_check_status",
                      "decode_attn_debug_gather",
                      "decode_attn_abi_version"):
             getattr(L, name).restype = ctypes.c_int
@@ -195,6 +198,22 @@ def decode_attn_run(plan, q: int, k_cache: int, v_cache: int, block_table: Optio
 
 def decode_attn_run_ex(plan, args: da_run_args):
     _check(lib().decode_attn_run_ex(plan, ctypes.byref(args)), "decode_attn_run_ex")
+
+
+def decode_attn_run_static(plan, q: int, k_cache: int, v_cache: int, block_table: Optional[int],
+                           seq_lens: int, scale: float, num_splits: int, out: int,
+                           out_lse: Optional[int], row_flags: Optional[int], stream: int = 0,
+                           want_stats: bool = False):
+    """decode_attn_run on the library's fixed per-device scratch: for callers that cannot
+    allocate a workspace. Pointers are integers (device addresses); nothing is allocated
+    here either. Returns da_stats when want_stats."""
+    st = da_stats() if want_stats else None
+    _check(lib().decode_attn_run_static(plan, q, k_cache, v_cache, block_table or None,
+                                        seq_lens, scale, num_splits, out, out_lse or None,
+                                        row_flags or None, stream or None,
+                                        ctypes.byref(st) if st is not None else None),
+           "decode_attn_run_static")
+    return st
 
 
 def decode_attn_check_status(plan, workspace: int, stream: int = 0):

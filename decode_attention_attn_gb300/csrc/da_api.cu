@@ -633,3 +633,77 @@ int decode_attn_debug_gather(const da_plan* plan, const int32_t* block_table,
 }
 
 }  // extern "C"
+
+// ---- decode_attn_run_static: the library's own fixed scratch in place of a workspace ----
+// One region per device, part of the library's device code: it is reserved (and zero-filled)
+// when that code is loaded on a device, never by a call.
+static __device__ __align__(256) unsigned char g_static_scratch[DECODE_ATTN_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxStaticDevices = 64;
+std::mutex g_static_mu;
+void* g_static_addr[kMaxStaticDevices] = {};
+
+// Device address of the current device's scratch region. Looked up on the first call made
+// with that device current (which loads the library's device code there if it is not yet
+// loaded) and cached for later calls.
+int static_scratch(void** addr) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxStaticDevices) return DA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+    g_static_addr[dev] = p;
+  }
+  *addr = g_static_addr[dev];
+  return DA_OK;
+}
+
+// decode_attn_run's host-side argument checks, made before the scratch is cleared so that
+// an argument error enqueues nothing.
+int static_args_ok(const da_plan& pl, const void* q, const void* k_cache, const void* v_cache,
+                   const int32_t* block_table, const int32_t* seq_lens, float scale,
+                   int num_splits, const void* out, const float* out_lse) {
+  if (!q || !k_cache || !v_cache || !seq_lens || !out) return DA_ERR_INVALID_ARG;
+  if (pl.prob.paged ? !block_table : block_table != nullptr) return DA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(seq_lens, 4) || !aligned(out, 16) || (out_lse && !aligned(out_lse, 4)) ||
+      (block_table && !aligned(block_table, 4)))
+    return DA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || num_splits < -1) return DA_ERR_INVALID_ARG;
+  if (num_splits == 0 && pl.batch_smem == 0) return DA_ERR_UNSUPPORTED;
+  if (num_splits > pl.max_splits) return DA_ERR_WORKSPACE_TOO_SMALL;
+  return DA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int decode_attn_run_static(const da_plan* plan, const void* q, const void* k_cache,
+                           const void* v_cache, const int32_t* block_table,
+                           const int32_t* seq_lens, float scale, int num_splits, void* out,
+                           float* out_lse, uint8_t* row_flags, void* cuda_stream,
+                           da_stats* stats) {
+  if (!plan) return DA_ERR_INVALID_ARG;
+  if (plan->ws_bytes > (size_t)DECODE_ATTN_STATIC_SCRATCH_BYTES) return DA_ERR_WORKSPACE_TOO_SMALL;
+  int rc = static_args_ok(*plan, q, k_cache, v_cache, block_table, seq_lens, scale, num_splits,
+                          out, out_lse);
+  if (rc != DA_OK) return rc;
+  void* scratch = nullptr;
+  rc = static_scratch(&scratch);
+  if (rc != DA_OK) return rc;
+  // The counters the kernels expect at zero: the region may hold another plan's layout.
+  rc = decode_attn_workspace_init(plan, scratch, DECODE_ATTN_STATIC_SCRATCH_BYTES, cuda_stream);
+  if (rc != DA_OK) return rc;
+  return decode_attn_run(plan, q, k_cache, v_cache, block_table, seq_lens, scale, num_splits,
+                         out, out_lse, row_flags, scratch, DECODE_ATTN_STATIC_SCRATCH_BYTES,
+                         cuda_stream, stats);
+}
+
+}  // extern "C"

@@ -200,6 +200,41 @@ typedef struct {
  * Errors: as decode_attn_run; INVALID_ARG also when only one event is given. */
 int decode_attn_run_ex(const da_plan* plan, const da_run_args* args);
 
+/* Size of the fixed scratch region that decode_attn_run_static uses (8 MiB per device). */
+#define DECODE_ATTN_STATIC_SCRATCH_BYTES (8u << 20)
+
+/* Run one decode step without a caller-provided workspace. The papers and pages this
+ * library follows have no counterpart to this entry point; it exists for callers that
+ * cannot allocate device memory for a workspace:
+ *   - a server whose device memory is reserved up front for the KV-cache pool;
+ *   - a process under a device-memory cap, where a new allocation can fail in mid-step;
+ *   - a decode loop that cannot afford cudaMalloc / cudaFree, which may synchronise the
+ *     whole device;
+ *   - plain C code with no device allocator of its own.
+ * In place of a workspace it uses one fixed region of DECODE_ATTN_STATIC_SCRATCH_BYTES per
+ * device, which belongs to the library's device code and is reserved when that code is
+ * loaded on the device. The call itself allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library routine.
+ *   Arguments as for decode_attn_run, less workspace and workspace_bytes.
+ *   First call on a device: it looks up the region's device address (with that device
+ *   current, as every call must have) and caches it, which can load the library's device
+ *   code on that device. Make the first call on each device before any stream capture.
+ *   Each call clears the region's counters on `cuda_stream` before the run, so runs of
+ *   different plans may follow one another on a stream.
+ *   Overlapping calls race: all calls on one device share the one region, so two calls
+ *   whose work can overlap on the GPU (other streams, other host threads, other plans)
+ *   corrupt each other's results. Serialise them, or use decode_attn_run with separate
+ *   workspaces.
+ * Errors: as decode_attn_run; WORKSPACE_TOO_SMALL also when the plan's workspace_bytes
+ * exceeds DECODE_ATTN_STATIC_SCRATCH_BYTES (use decode_attn_run with a workspace of that
+ * size instead); UNSUPPORTED on a device with ordinal 64 or above. Argument errors are
+ * detected before anything is enqueued. */
+int decode_attn_run_static(const da_plan* plan, const void* q, const void* k_cache,
+                           const void* v_cache, const int32_t* block_table,
+                           const int32_t* seq_lens, float scale, int num_splits, void* out,
+                           float* out_lse, uint8_t* row_flags, void* cuda_stream,
+                           da_stats* stats);
+
 /* Synchronise `stream`, then read and clear the device findings recorded in the
  * workspace by earlier runs. Returns DA_OK or the first finding's DA_ERR_* code. */
 int decode_attn_check_status(const da_plan* plan, void* workspace, void* cuda_stream);
