@@ -464,7 +464,8 @@ int decode_attn_run_ex(const da_plan* plan, const da_run_args* args) {
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
   const bool unified = p.mode == DA_SOFTMAX_UNIFIED;
 
-  const bool mma = uses_mma(pl.es, p.qkv_dtype == DA_BF16, pl.group, unified);
+  // tensor-core kernels (both modes, so the recompute pass too) read 128-byte-swizzled tiles
+  const bool mma = uses_mma(pl.es, p.qkv_dtype == DA_BF16, pl.group);
   CUtensorMap tmk, tmv;
   int rc = make_kv_map(pl, k_cache, mma, &tmk);
   if (rc == DA_OK) rc = make_kv_map(pl, v_cache, mma, &tmv);
@@ -575,13 +576,7 @@ int decode_attn_run_ex(const da_plan* plan, const da_run_args* args) {
         pl.num_sms, (long long)pl.n_groups * pl.recompute_splits));
     rcfg.attrs = pdl;
     rcfg.numAttrs = 1;
-    CUtensorMap rk = tmk, rv = tmv;   // the recompute runs CUDA-core consumers: plain tiles
-    if (mma) {
-      rc = make_kv_map(pl, k_cache, false, &rk);
-      if (rc == DA_OK) rc = make_kv_map(pl, v_cache, false, &rv);
-      if (rc != DA_OK) return rc;
-    }
-    void* rargs[3] = {&rp, &rk, &rv};
+    void* rargs[3] = {&rp, &tmk, &tmv};   // same consumer kind, same tile layout
     e = cudaLaunchKernelExC(&rcfg, rfn, rargs);
     if (e != cudaSuccess) return cuda_fail(e, "launching the recompute kernel");
   }

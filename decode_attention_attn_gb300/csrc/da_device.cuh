@@ -97,11 +97,11 @@ struct Layout {
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-// Split kernels whose unified-max consumers run on the tensor cores (see da_mma.cuh): bf16
-// caches, packed groups of 4 or 8 query heads. Their K/V tiles are TMA-loaded with the 128-byte
-// swizzle (4-D view: 64-element rows, d / 64 of them per token, heads, tokens).
-__host__ __device__ constexpr bool uses_mma(int es, bool is_bf16, int G, bool unified) {
-  return unified && es == 2 && is_bf16 && (G == 4 || G == 8);
+// Split kernels whose consumers run on the tensor cores (see da_mma.cuh), in either softmax
+// mode: bf16 caches, packed groups of 4 or 8 query heads. Their K/V tiles are TMA-loaded with
+// the 128-byte swizzle (4-D view: 64-element rows, d / 64 of them per token, heads, tokens).
+__host__ __device__ constexpr bool uses_mma(int es, bool is_bf16, int G) {
+  return es == 2 && is_bf16 && (G == 4 || G == 8);
 }
 
 // Geometry of a consumer warp's logit transpose: a KV row of D elements of es bytes is split

@@ -513,7 +513,7 @@ __device__ __forceinline__ void publish_cuda(const LaneMap<T, D, G>& lm,
 
 // Publish a tensor-core warp's piece state (same scratch format as publish_cuda).
 template <typename T, int D, int G>
-__device__ __forceinline__ void publish_mma(const MmaState<D, G>& st, float phi2, uint32_t fmask,
+__device__ __forceinline__ void publish_mma(const MmaState<D, G>& st, float m, uint32_t fmask,
                                             float* mm, float* ml, uint32_t* mflag, float* wbuf,
                                             int warp, int lane) {
   constexpr int W = warp_scratch_floats(D, G, (int)sizeof(T));
@@ -529,7 +529,7 @@ __device__ __forceinline__ void publish_mma(const MmaState<D, G>& st, float phi2
       wbuf[warp * W + head * D + 8 * j + c0 + 1] = st.o[j][1];
     }
     if ((lane & 3) == 0) {
-      mm[warp * G + head] = phi2;
+      mm[warp * G + head] = m;
       ml[warp * G + head] = den;
     }
   }
@@ -765,7 +765,7 @@ __device__ __forceinline__ void run_consumers(const Params& p, Sched s, uint8_t*
 
 // Tensor-core consumers (unified softmax, bf16, G >= 4): same stage-pair loop as
 // run_consumers, the math in mma_consume.
-template <typename T, int D, int G>
+template <typename T, int D, int G, bool UNIFIED>
 __device__ __forceinline__ void run_consumers_mma(const Params& p, Sched s, uint8_t* stages,
                                                   const Layout& L, uint64_t* full,
                                                   uint64_t* empty, uint8_t* smem, int warp,
@@ -788,6 +788,7 @@ __device__ __forceinline__ void run_consumers_mma(const Params& p, Sched s, uint
 #pragma unroll
       for (int i = 0; i < 4; ++i) st.o[j][i] = 0.f;
     st.den = 0.f;
+    st.m = -INFINITY;
     uint32_t fmask = 0;
     const int nst = (pc.t1 - pc.t0 + kStageTokens - 1) / kStageTokens;
     for (int j = 0; j < nst; j += 2) {
@@ -809,7 +810,7 @@ __device__ __forceinline__ void run_consumers_mma(const Params& p, Sched s, uint
                         pair ? min(kStageTokens, pc.t1 - ts - kStageTokens) : 0};
       const uint8_t* const kss[2] = {st0 + L.k_off, st1 + L.k_off};
       const uint8_t* const vss[2] = {st0 + L.v_off, st1 + L.v_off};
-      if (!dead) mma_consume<D, G>(p, st, kss, vss, n, row0, lane, fmask);
+      if (!dead) mma_consume<D, G, UNIFIED>(p, st, kss, vss, n, row0, lane, fmask);
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&empty[s0]);
@@ -817,7 +818,7 @@ __device__ __forceinline__ void run_consumers_mma(const Params& p, Sched s, uint
       }
       k += pair ? 2u : 1u;
     }
-    publish_mma<T, D, G>(st, p.phi2, fmask, mm, ml, mflag, wbuf, warp, lane);
+    publish_mma<T, D, G>(st, UNIFIED ? p.phi2 : st.m, fmask, mm, ml, mflag, wbuf, warp, lane);
     combine_piece<T, D, G>(p, pc, mm, ml, mflag, wbuf, misc, warp, lane, ctid);
   }
 }
@@ -921,11 +922,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Registers move from the producer warpgroup (one working warp) to the two consumer
   // warpgroups: 8 * 32 * kConsumerRegs + 4 * 32 * kProducerRegs equals the launch's
   // 12 * 32 * 168 (checked on the host before the first launch).
-  constexpr bool kMma = uses_mma(sizeof(T), std::is_same<T, __nv_bfloat16>::value, G, UNIFIED);
+  constexpr bool kMma = uses_mma(sizeof(T), std::is_same<T, __nv_bfloat16>::value, G);
   if (warp < kConsumerWarps) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
     if constexpr (kMma)
-      run_consumers_mma<T, D, G>(p, s, stages, L, full, empty, smem, warp, lane);
+      run_consumers_mma<T, D, G, UNIFIED>(p, s, stages, L, full, empty, smem, warp, lane);
     else
       run_consumers<T, D, G, UNIFIED>(p, s, stages, L, full, empty, smem, warp, lane);
   } else {

@@ -1,5 +1,5 @@
-// da_mma.cuh -- tensor-core consumer of the unified-max (asynchronised) softmax for packed
-// GQA groups of G >= 4 query heads over bf16 caches.
+// da_mma.cuh -- tensor-core consumer for packed GQA groups of G >= 4 query heads over bf16
+// caches, in both softmax modes.
 //
 // Per KV tile the group's work is two dense contractions ([G x d] . [d x T] for the logits,
 // [G x T] . [T x d] for P . V). On CUDA cores they made the split kernel ALU-bound on GB300
@@ -10,10 +10,13 @@
 //   128-byte-swizzled TMA tile with ldmatrix;
 //   O += P V: A = P taken straight from the S accumulators (rows = heads, k = tokens), B = V
 //   rows read transposed with ldmatrix.trans.
-// With one constant phi (FlashDecoding++ Eq. 3 / Eq. 4) the accumulators are never rescaled,
-// so O accumulates in the MMA registers across the whole piece. P enters the MMA as a bf16
-// pair p_hi + p_lo (p_lo = bf16 of the rounding residual), which keeps P exact to ~2^-17;
-// the softmax denominators are summed from the FP32 p.
+// O accumulates in the MMA registers across the whole piece. With one constant phi
+// (FlashDecoding++ Eq. 3 / Eq. 4) the accumulators are never rescaled. In the synchronised
+// mode each warp keeps a running maximum per head (the online-softmax recurrence of
+// "FlashAttention: tiling plus online softmax"); when one of them grows the warp rescales its
+// accumulators and denominators by 2^(m_old - m_new), which after the first tiles is rare.
+// P enters the MMA as a bf16 pair p_hi + p_lo (p_lo = bf16 of the rounding residual), which
+// keeps P exact to ~2^-17; the softmax denominators are summed from the FP32 p.
 //
 // Each consumer warp takes 8 rows of two consecutive stages (16 tokens = one MMA k-extent).
 #pragma once
@@ -71,6 +74,7 @@ struct MmaState {
   uint32_t qa[KS][2];                   // A fragments of q (a0, a2); rows 8..15 are zero
   float o[NT][4];                       // O accumulators (rows = heads; rows >= G unused)
   float den;                            // this lane's share of its head's denominator
+  float m;                              // synchronised mode: its head's running maximum
 };
 
 // Load the group's q fragments from the stage's q area (G x D bf16, row-major, unscaled).
@@ -88,7 +92,7 @@ __device__ __forceinline__ void mma_load_q(MmaState<D, G>& st, const uint8_t* qs
 
 // Consume the warp's 8 rows of two consecutive stages (n[1] == 0: no second stage; its rows are
 // masked and read stage 0's tile instead, so no stale shared memory enters the MMA).
-template <int D, int G>
+template <int D, int G, bool UNIFIED>
 __device__ __forceinline__ void mma_consume(const Params& p, MmaState<D, G>& st,
                                             const uint8_t* const (&ks)[2],
                                             const uint8_t* const (&vs)[2], const int (&n)[2],
@@ -115,19 +119,50 @@ __device__ __forceinline__ void mma_consume(const Params& p, MmaState<D, G>& st,
     }
   }
 
-  // unified-max softmax on the accumulator elements this lane holds: head lane/4, tokens
-  // 2 (lane % 4) + {0, 1} of each stage
+  // softmax on the accumulator elements this lane holds: head lane/4, tokens
+  // 2 (lane % 4) + {0, 1} of each stage; the quad of lanes 4h..4h+3 holds head h's 16 logits
   const int head = lane >> 2, tk = 2 * (lane & 3);
   const bool hv = head < G;
+  float x[2][2];
+  bool valid[2][2];
+#pragma unroll
+  for (int b = 0; b < 2; ++b)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      x[b][e] = s[b][e] * p.qscale;
+      valid[b][e] = hv && row0 + tk + e < n[b];
+    }
+  float ref = p.phi2;
+  if constexpr (!UNIFIED) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int b = 0; b < 2; ++b)
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+        if (valid[b][e]) mx = fmaxf(mx, x[b][e]);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float m_new = fmaxf(st.m, mx);
+    if (__any_sync(0xffffffffu, m_new > st.m)) {
+      const float alpha = m_new > st.m ? fast_exp2(st.m - m_new) : 1.f;   // 0 from -inf
+#pragma unroll
+      for (int j = 0; j < MmaState<D, G>::NT; ++j) {
+        st.o[j][0] *= alpha;   // rows 8..15 ([2], [3]) stay zero
+        st.o[j][1] *= alpha;
+      }
+      st.den *= alpha;
+      st.m = m_new;
+    }
+    ref = st.m;   // -inf only while all of the head's tokens so far are masked
+  }
   float pr[2][2];
 #pragma unroll
   for (int b = 0; b < 2; ++b)
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const float x = s[b][e] * p.qscale;
-      const bool valid = hv && row0 + tk + e < n[b];
-      pr[b][e] = valid ? fast_exp2(x - p.phi2) : 0.f;
-      if (valid && (x < p.lo2 || x > p.hi2)) fmask |= 1u << head;
+      pr[b][e] = valid[b][e] ? fast_exp2(x[b][e] - ref) : 0.f;
+      if constexpr (UNIFIED)
+        if (valid[b][e] && (x[b][e] < p.lo2 || x[b][e] > p.hi2)) fmask |= 1u << head;
       st.den += pr[b][e];
     }
   // P as A fragments (k = token: stage 0 rows in k 0..7, stage 1 rows in k 8..15), hi + lo
