@@ -51,7 +51,7 @@ using namespace da;
 struct da_plan {
   da_problem prob;
   int num_sms;
-  int group, es, unit, box_tokens, capacity, n_groups;
+  int group, es, unit, box_tokens, capacity, n_groups, piece_units;
   int policy, num_splits;       // the plan's default split choice
   int grid;                     // balanced grid (or the default uniform grid)
   int recompute_splits, max_splits;
@@ -236,6 +236,7 @@ void fill_common(const da_plan& pl, Params& k, const int32_t* block_table,
   k.max_seq_len = p.paged ? 0 : p.max_seq_len;
   k.capacity = pl.capacity;
   k.unit = pl.unit;
+  k.piece_units = pl.piece_units;
   k.box_tokens = pl.box_tokens;
   k.out_dtype = p.out_dtype;
   k.n_groups = pl.n_groups;
@@ -297,6 +298,10 @@ int decode_attn_plan(const da_problem* problem, int num_splits, da_plan** plan_o
   pl->box_tokens = p.paged ? std::min(p.page_size, kStageTokens) : kStageTokens;
   pl->capacity = p.paged ? p.max_blocks_per_seq * p.page_size : p.max_seq_len;
   pl->n_groups = p.batch * p.num_kv_heads;
+  {
+    const long long unit_bytes = 2LL * pl->unit * p.head_dim * pl->es;   // K + V of one unit
+    pl->piece_units = (int)((kPieceCostBytes + unit_bytes / 2) / unit_bytes);
+  }
   const long long units_max = (pl->capacity + pl->unit - 1) / pl->unit;
   const long long w_max = (long long)pl->n_groups * units_max;
   pl->batch_smem = p.batch <= kMaxBatchSmem ? p.batch : 0;

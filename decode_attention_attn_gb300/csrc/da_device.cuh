@@ -26,6 +26,11 @@ constexpr int kMaxStages = 8;
 constexpr int kMaxBatchSmem = 2048;                     // balanced schedule keeps B lengths in smem
 constexpr uint32_t kSmemLimit = 232448;                 // 227 KB opt-in per CTA
 constexpr int kMinUnitsPerCta = 8;                      // no share below 8 units (128 tokens)
+// Balanced shares charge every piece this many K+V bytes on top of its tokens: a piece ends
+// with an in-CTA combine during which the CTA's copy stream stalls (about 2 us, measured as
+// the end-time slope of CTAs over their piece counts), so CTAs whose share spans many short
+// sequences would otherwise finish last.
+constexpr int kPieceCostBytes = 96 * 1024;
 
 // status bits recorded by the device in the workspace
 constexpr int kStatusBadBlockTable = 1;
@@ -58,6 +63,7 @@ struct Params {
   int paged, page_size, max_blocks, num_blocks, max_seq_len;
   int capacity;                  // token capacity of one sequence
   int unit;                      // split boundaries fall on multiples of this many tokens
+  int piece_units;               // balanced: cost units charged per group ahead of its tokens
   int box_tokens;                // KV rows per TMA box
   int out_dtype;
   int policy;                    // kBalanced / kUniform

@@ -101,7 +101,7 @@ struct Sched {
   long long i, i1;       // uniform: item cursor, end
   int S;
   const int* lens;       // balanced: clamped lengths (smem)
-  const int* prefix;     // balanced: exclusive prefix of units per sequence (smem)
+  const int* prefix;     // balanced: exclusive prefix of per-head units (cost + tokens) (smem)
 };
 
 __device__ __forceinline__ int clamp_len(const Params& p, int n) {
@@ -115,33 +115,40 @@ __device__ __forceinline__ long long cta_of(long long u, long long W, int P) {
 
 __device__ __forceinline__ bool sched_next(Sched& s, const Params& p, Piece& pc) {
   if (s.policy == kBalanced) {
-    if (s.u >= s.u1) return false;
-    const long long u = s.u;
-    const long long hkv = p.hkv;
-    int lo = 0, hi = p.batch;   // invariant: hkv * prefix[lo] <= u < hkv * prefix[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (hkv * s.prefix[mid] <= u) lo = mid; else hi = mid;
+    // Group g of sequence b owns units [gs, ge) of the step's unit space: piece_units cost
+    // units, then one per `unit` tokens. A share that holds only cost units of a group has no
+    // piece of it.
+    while (s.u < s.u1) {
+      const long long u = s.u;
+      const long long hkv = p.hkv;
+      int lo = 0, hi = p.batch;   // invariant: hkv * prefix[lo] <= u < hkv * prefix[hi]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (hkv * s.prefix[mid] <= u) lo = mid; else hi = mid;
+      }
+      const int b = lo;
+      const long long nb = s.prefix[b + 1] - s.prefix[b];
+      const long long base = hkv * s.prefix[b];
+      const int kvh = (int)((u - base) / nb);
+      const long long gs = base + kvh * nb, ge = gs + nb;
+      const long long rs = gs + p.piece_units;   // the group's first token unit
+      const long long pe = s.u1 < ge ? s.u1 : ge;
+      s.u = pe;
+      if (pe <= rs) continue;
+      const long long n = s.lens[b];
+      pc.b = b;
+      pc.kvh = kvh;
+      pc.g = b * p.hkv + kvh;
+      pc.t0 = (int)(((u > rs ? u : rs) - rs) * p.unit);
+      const long long t1 = (pe - rs) * p.unit;
+      pc.t1 = (int)(t1 < n ? t1 : n);
+      const long long cf = cta_of(rs, s.W, s.P), cl = cta_of(ge - 1, s.W, s.P);
+      pc.nslots = (int)(cl - cf + 1);
+      pc.slot_base = (int)cf + pc.g;
+      pc.slot = s.c + pc.g;
+      return true;
     }
-    const int b = lo;
-    const long long nb = s.prefix[b + 1] - s.prefix[b];
-    const long long base = hkv * s.prefix[b];
-    const int kvh = (int)((u - base) / nb);
-    const long long gs = base + kvh * nb, ge = gs + nb;
-    const long long pe = s.u1 < ge ? s.u1 : ge;
-    const long long n = s.lens[b];
-    pc.b = b;
-    pc.kvh = kvh;
-    pc.g = b * p.hkv + kvh;
-    pc.t0 = (int)((u - gs) * p.unit);
-    const long long t1 = (pe - gs) * p.unit;
-    pc.t1 = (int)(t1 < n ? t1 : n);
-    const long long cf = cta_of(gs, s.W, s.P), cl = cta_of(ge - 1, s.W, s.P);
-    pc.nslots = (int)(cl - cf + 1);
-    pc.slot_base = (int)cf + pc.g;
-    pc.slot = s.c + pc.g;
-    s.u = pe;
-    return true;
+    return false;
   }
   if (s.i >= s.i1) return false;
   const long long i = s.i++;
@@ -874,7 +881,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int per = (p.batch + 31) / 32;
       const int beg = min(p.batch, lane * per), end = min(p.batch, beg + per);
       int local = 0;
-      for (int b = beg; b < end; ++b) local += (lens[b] + p.unit - 1) / p.unit;
+      for (int b = beg; b < end; ++b)
+        local += lens[b] ? (lens[b] + p.unit - 1) / p.unit + p.piece_units : 0;
       int incl = local;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -884,14 +892,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       int run = incl - local;
       for (int b = beg; b < end; ++b) {
         prefix[b] = run;
-        run += (lens[b] + p.unit - 1) / p.unit;
+        run += lens[b] ? (lens[b] + p.unit - 1) / p.unit + p.piece_units : 0;
       }
       if (lane == 31) prefix[p.batch] = incl;
     }
     __syncthreads();
     s.W = (long long)p.hkv * prefix[p.batch];
-    s.u = (long long)blockIdx.x * s.W / gridDim.x;
-    s.u1 = ((long long)blockIdx.x + 1) * s.W / gridDim.x;
+    // The grid is sized from the cache capacity; when the step holds fewer units than CTAs,
+    // only the first W CTAs take shares, so that every share is non-empty and a group's
+    // pieces sit on consecutive CTAs (its piece count is then cl - cf + 1).
+    s.P = (int)(s.W < (long long)gridDim.x ? s.W : (long long)gridDim.x);
+    if ((int)blockIdx.x < s.P) {
+      s.u = (long long)blockIdx.x * s.W / s.P;
+      s.u1 = ((long long)blockIdx.x + 1) * s.W / s.P;
+    }
     // sequences with no tokens have no piece: out = 0, lse = -inf, flag = 0
     for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
       if (lens[b] != 0) continue;

@@ -135,6 +135,31 @@ def test_edge_sweep(dtype, head_dim, group):
                        where=f"edge {dtype} d{head_dim} G{group} paged={paged} S={ns}")
 
 
+@pytest.mark.parametrize("group", [1, 4])
+@pytest.mark.parametrize("paged", [False, True])
+def test_step_with_fewer_units_than_ctas(group, paged):
+    """The grid is sized from the cache capacity (8192 tokens here) but this step holds a few
+    dozen 16-token units, fewer than the CTAs: balanced shares must still put each group's
+    pieces on consecutive CTAs, so that the merge finds every partial it counts."""
+    lens = (40, 0, 100, 0, 1)
+    wl = workloads.Workload(f"sparse_G{group}_paged{paged}", len(lens), 2 * group, 2, 128,
+                            "bf16", "bf16", lens=lens, paged=paged, page_size=16,
+                            max_seq_len=0 if paged else 8192)
+    inp = workloads.generate(wl, offset=11 + group)
+    if paged:   # a wide table: the capacity, not the lengths, sizes the grid
+        bt = torch.full((len(lens), 512), -1, dtype=torch.int32)
+        bt[:, :inp.block_table.shape[1]] = inp.block_table
+        inp.block_table, inp.max_blocks_per_seq = bt, 512
+    dev = _parity.DeviceInputs(inp)
+    ref, ref_lse, _, _ = _parity.run_oracle(inp)
+    attn = binding.DecodeAttention(_parity.problem_for(inp), 0)
+    assert attn.info.grid_ctas >= 100   # this step has fewer than 100 units, cost units included
+    for mode in ("sync", "unified"):
+        for od in ("bf16", "f32"):
+            _check(dev, ref, ref_lse, mode, out_dtype=od, num_splits=0, plan_splits=0,
+                   where=f"sparse G{group} paged={paged}")
+
+
 @pytest.mark.parametrize("page_size", [8, 16, 32, 64, 128])
 def test_page_sizes(page_size):
     wl = workloads.PAGED_B64.replace(name=f"pages{page_size}", batch=6, page_size=page_size,
