@@ -253,6 +253,10 @@ class DecodeAttention:
         self.problem = problem
         self.plan, self.workspace_bytes = decode_attn_plan(problem, num_splits)
         self.info = decode_attn_plan_info(self.plan)
+        from .workloads import TORCH_DTYPES
+        names = {v: k for k, v in DTYPE_CODES.items()}
+        self._qkv_dtype = TORCH_DTYPES[names[problem.qkv_dtype]]
+        self._out_dtype = TORCH_DTYPES[names[problem.out_dtype]]
         self.device = torch.device(device) if device is not None else torch.device("cuda")
         # a zero-filled workspace needs no decode_attn_workspace_init call
         self.workspace = torch.zeros(self.workspace_bytes, dtype=torch.uint8, device=self.device)
@@ -267,10 +271,8 @@ class DecodeAttention:
             out=None, out_lse=None, row_flags=None, stream=None, want_stats: bool = False,
             split_events=None):
         import torch
-        from .workloads import TORCH_DTYPES
         pr = self.problem
-        names = {v: k for k, v in DTYPE_CODES.items()}
-        qkv = TORCH_DTYPES[names[pr.qkv_dtype]]
+        qkv = self._qkv_dtype
         for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
             if t.device.type != "cuda" or t.dtype != qkv or not t.is_contiguous():
                 raise ValueError(f"{name} must be a contiguous CUDA tensor of {qkv}")
@@ -281,8 +283,7 @@ class DecodeAttention:
             raise ValueError("block_table must be a contiguous int32 CUDA tensor")
         B, H = pr.batch, pr.num_q_heads
         if out is None:
-            out = torch.empty((B, H, pr.head_dim), dtype=TORCH_DTYPES[names[pr.out_dtype]],
-                              device=q.device)
+            out = torch.empty((B, H, pr.head_dim), dtype=self._out_dtype, device=q.device)
         if out_lse is None:
             out_lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
         if row_flags is None:

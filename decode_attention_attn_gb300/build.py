@@ -1,8 +1,7 @@
 """Build libdecode_attn.so (the C-ABI CUDA library) in-tree for sm_103a.
 
-Five translation units (the host API, the merge kernel and one split-kernel instantiation
-unit per storage type)
-are compiled in parallel with nvcc and linked into decode_attention_attn_gb300/_lib/.
+Four translation units (the host API and one split-kernel instantiation unit per storage
+type) are compiled in parallel with nvcc and linked into decode_attention_attn_gb300/_lib/.
 """
 import concurrent.futures
 import os
@@ -16,8 +15,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libdecode_attn.so")
-SOURCES = ["da_api.cu", "da_merge.cu", "da_kernels_f32.cu", "da_kernels_f16.cu",
-           "da_kernels_bf16.cu"]
+SOURCES = ["da_api.cu", "da_kernels_f32.cu", "da_kernels_f16.cu", "da_kernels_bf16.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-I" + INCLUDE, "-I" + CSRC]

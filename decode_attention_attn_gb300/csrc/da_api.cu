@@ -21,7 +21,6 @@ namespace da {
 const void* kernel_f32(int head_dim, int group, bool unified);
 const void* kernel_f16(int head_dim, int group, bool unified);
 const void* kernel_bf16(int head_dim, int group, bool unified);
-const void* merge_kernel_ptr();
 
 // The element offset the kernel reads token t of (b, kvh) from: the same token_row() the
 // producer warp uses for its TMA box coordinates.
@@ -58,7 +57,7 @@ struct da_plan {
   int stages, batch_smem;
   size_t smem_bytes;
   long long slots;
-  size_t off_counters, off_list, off_list_state, off_status, off_stats, off_desc;
+  size_t off_counters, off_list, off_list_state, off_status, off_stats;
   size_t off_part_flags, off_part_l, off_part_o, zero_bytes, ws_bytes;
 };
 
@@ -139,12 +138,6 @@ int ensure_smem_attr(const void* fn, size_t smem) {
       return DA_ERR_CUDA;
     }
   }
-  // Every kernel of a run asks for the maximal shared-memory carveout, so that the merge
-  // kernel's CTAs can share an SM with the split kernel's instead of waiting for a reconfigure.
-  e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           (int)cudaSharedmemCarveoutMaxShared);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(carveout)");
-  (void)smem;
   g_attr_done.insert({dev, fn});
   return DA_OK;
 }
@@ -222,7 +215,6 @@ void fill_common(const da_plan& pl, Params& k, const int32_t* block_table,
     k.part_flags = reinterpret_cast<uint32_t*>(w + pl.off_part_flags);
     k.part_l = reinterpret_cast<float*>(w + pl.off_part_l);
     k.part_o = reinterpret_cast<float*>(w + pl.off_part_o);
-    k.desc = reinterpret_cast<int2*>(w + pl.off_desc);
   }
   k.batch = p.batch;
   k.hq = p.num_q_heads;
@@ -357,13 +349,11 @@ int decode_attn_plan(const da_problem* problem, int num_splits, da_plan** plan_o
   off = align256(off + (size_t)pl->n_groups * 4);
   pl->off_list = off;
   off = align256(off + (size_t)pl->n_groups * 4);
-  pl->off_list_state = off;
-  pl->off_status = off + 8;
-  pl->off_stats = off + 16;
-  off = align256(off + 32);
+  pl->off_list_state = off;      // 2 x int32
+  pl->off_status = off + 16;     // int32
+  pl->off_stats = off + 24;      // 2 x uint64
+  off = align256(off + 40);
   pl->zero_bytes = off;
-  pl->off_desc = off;
-  off = align256(off + (size_t)pl->n_groups * 8);
   pl->off_part_flags = off;
   off = align256(off + (size_t)pl->slots * 4);
   pl->off_part_l = off;
@@ -484,8 +474,6 @@ int decode_attn_run_ex(const da_plan* plan, const da_run_args* args) {
   kp.row_flags = row_flags;
   kp.policy = policy;
   kp.num_splits = S;
-  kp.use_list = 0;
-  kp.write_flags = 1;
   const double log2e = 1.4426950408889634;
   kp.qscale = (float)((double)scale * log2e);
   kp.phi2 = (float)((double)p.unified_max * log2e);
@@ -503,6 +491,7 @@ int decode_attn_run_ex(const da_plan* plan, const da_run_args* args) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(status)");
   }
 
+  // The split kernel computes the step; the last piece of each group merges it in-kernel.
   const void* fn = kernel_for(pl, unified);
   if (!fn) return DA_ERR_UNSUPPORTED;
   rc = ensure_smem_attr(fn, pl.smem_bytes);
@@ -524,58 +513,20 @@ int decode_attn_run_ex(const da_plan* plan, const da_run_args* args) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(split_event_end)");
   }
 
-  cudaLaunchAttribute pdl[1];
-  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  pdl[0].val.programmaticStreamSerializationAllowed = 1;
-  {
-    // Merge of the groups split into several pieces, as a programmatic dependent without
-    // shared memory: its CTAs wait beside the split kernel's and start when its writes land.
-    MergeParams mp;
-    std::memset(&mp, 0, sizeof mp);
-    mp.out = out;
-    mp.out_lse = out_lse;
-    mp.row_flags = row_flags;
-    mp.part_o = kp.part_o;
-    mp.part_l = kp.part_l;
-    mp.part_flags = kp.part_flags;
-    mp.desc = kp.desc;
-    mp.flag_list = kp.flag_list;
-    mp.list_state = kp.list_state;
-    mp.stats = kp.stats;
-    mp.n_groups = pl.n_groups;
-    mp.rows_per_group = pl.group;
-    mp.head_dim = p.head_dim;
-    mp.out_dtype = p.out_dtype;
-    mp.write_flags = 1;
-    const long long items = (long long)pl.n_groups * pl.group * (p.head_dim / 32);
-    cudaLaunchConfig_t mcfg = {};
-    mcfg.gridDim = dim3((unsigned)std::max<long long>(
-        1, std::min<long long>((items + 3) / 4, (long long)pl.num_sms * 4)));
-    mcfg.blockDim = dim3(128);
-    mcfg.dynamicSmemBytes = 0;
-    mcfg.stream = stream;
-    mcfg.attrs = pdl;
-    mcfg.numAttrs = 1;
-    void* margs[1] = {&mp};
-    rc = ensure_smem_attr(merge_kernel_ptr(), 0);
-    if (rc != DA_OK) return rc;
-    e = cudaLaunchKernelExC(&mcfg, merge_kernel_ptr(), margs);
-    if (e != cudaSuccess) return cuda_fail(e, "launching the merge kernel");
-  }
-
   if (unified) {
-    // Synchronised recompute of flagged groups ("The Overflow Fallback: Recomputation").
-    // Always enqueued, as a programmatic dependent of the merge, so that no host round trip
-    // is needed; it exits at once when nothing was flagged. Its pieces merge in-kernel.
+    // Synchronised recompute of flagged groups ("The Overflow Fallback: Recomputation"),
+    // always enqueued, as a programmatic dependent of the split kernel, so that no host round
+    // trip is needed; it exits at once when nothing was flagged.
     Params rp = kp;
     rp.policy = kUniform;
     rp.num_splits = pl.recompute_splits;
-    rp.use_list = 1;
-    rp.write_flags = 0;
-    rp.inline_merge = 1;
+    rp.recompute = 1;
     const void* rfn = kernel_for(pl, false);
     rc = ensure_smem_attr(rfn, pl.smem_bytes);
     if (rc != DA_OK) return rc;
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t rcfg = cfg;
     rcfg.gridDim = dim3((unsigned)std::min<long long>(
         pl.num_sms, (long long)pl.n_groups * pl.recompute_splits));

@@ -51,8 +51,9 @@ struct Params {
   float* out_lse;                // [B, Hq] or null
   uint8_t* row_flags;            // [B, Hq] or null
   int32_t* counters;             // [n_groups] arrivals per group (self-cleaning)
-  int32_t* flag_list;            // [n_groups] flagged groups (unified main pass)
-  int32_t* list_state;           // [0] flagged count, [1] recompute CTAs finished
+  int32_t* flag_list;            // [n_groups] flagged groups (unified mode)
+  int32_t* list_state;           // unified: [0] flagged count, [1] recompute CTAs finished
+                                 // (self-cleaning)
   int32_t* status;               // device findings
   unsigned long long* stats;     // [0] rows flagged, [1] split partials flagged
   uint32_t* part_flags;          // [slots] range-check bits per head
@@ -68,30 +69,12 @@ struct Params {
   int out_dtype;
   int policy;                    // kBalanced / kUniform
   int num_splits;                // uniform: splits per group
-  int use_list;                  // recompute pass: groups come from flag_list
-  int write_flags;               // main unified pass: flags, flagged list, stats
+  int recompute;                 // 1: the recompute launch (groups from the flagged list)
   int n_groups;                  // B * Hkv
   int stages;                    // pipeline depth
   int batch_smem;                // lengths held in smem (balanced) or 0
   float qscale;                  // scale * log2(e): logits come out in log2 units
   float phi2, lo2, hi2;          // unified constant and range bounds, log2 units
-  int2* desc;                    // [n_groups] (first partial slot, pieces) of each group
-  int inline_merge;              // 1: the last piece of a group merges it (recompute pass)
-};
-
-// Launch parameters of the merge kernel (one warp per (group, row, 32-wide d chunk)).
-struct MergeParams {
-  void* out;
-  float* out_lse;
-  uint8_t* row_flags;
-  const float* part_o;
-  const float* part_l;
-  const uint32_t* part_flags;
-  const int2* desc;
-  int32_t* flag_list;
-  int32_t* list_state;
-  unsigned long long* stats;
-  int n_groups, rows_per_group, head_dim, out_dtype, write_flags;
 };
 
 // ---- shared-memory layout (host and device compute it identically) ------------------------

@@ -100,6 +100,8 @@ struct Sched {
   int P, c;
   long long i, i1;       // uniform: item cursor, end
   int S;
+  bool use_list;         // uniform: item i / S indexes the flagged list, not the groups
+  bool first_phase;      // the step's first pass (flags, statistics, flagged list)
   const int* lens;       // balanced: clamped lengths (smem)
   const int* prefix;     // balanced: exclusive prefix of per-head units (cost + tokens) (smem)
 };
@@ -153,7 +155,7 @@ __device__ __forceinline__ bool sched_next(Sched& s, const Params& p, Piece& pc)
   if (s.i >= s.i1) return false;
   const long long i = s.i++;
   const int li = (int)(i / s.S), sp = (int)(i % s.S);
-  const int g = p.use_list ? __ldcg(p.flag_list + li) : li;
+  const int g = s.use_list ? __ldcg(p.flag_list + li) : li;
   const int b = g / p.hkv;
   const int n = clamp_len(p, __ldg(p.seq_lens + b));
   const int ts = n == 0 ? 0 : ((n + s.S - 1) / s.S + p.unit - 1) / p.unit * p.unit;
@@ -178,13 +180,12 @@ template <typename T, int D, int G, bool SWZ>
 __device__ __forceinline__ void run_producer(const Params& p, Sched s, uint8_t* stages,
                                              const Layout& L, uint64_t* full, uint64_t* empty,
                                              const CUtensorMap* tmk, const CUtensorMap* tmv,
-                                             int lane, int part) {
+                                             int lane, int part, uint32_t& k, bool& dead) {
   using C = Cfg<T, D, G>;
   const uint64_t pol = make_evict_first_policy();
   const uint32_t NS = (uint32_t)p.stages;
   const int nsub = p.paged ? 2 : 1;   // warps per tensor: K from even parts, V from odd
-  uint32_t k = 0, issued = 0;   // stages passed / one past the last stage with copies
-  bool dead = false;
+  uint32_t issued = 0;   // one past the last stage this call issued copies for
   Piece pc;
   while (sched_next(s, p, pc)) {
     if (pc.t1 <= pc.t0) continue;
@@ -375,7 +376,7 @@ __device__ __forceinline__ void consume_stages(const Params& p, const LaneMap<T,
   if constexpr (UNIFIED) {
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
-        float2* pw = pwarp + b * kTokensPerWarp * G + lm.lg * C::kV;
+      float2* pw = pwarp + b * kTokensPerWarp * G + lm.lg * C::kV;
 #pragma unroll
       for (int i = 0; i < C::kNv; ++i) {
         const float s = sc[b][i];
@@ -544,11 +545,15 @@ __device__ __forceinline__ void publish_mma(const MmaState<D, G>& st, float m, u
 }
 
 // The 8 consumer warps' published states -> one partial (or the output, when the piece is
-// its group's only one); the recompute pass merges its own pieces here.
+// its group's only one). The last piece of a group to finish merges the group's partials
+// here (the split-KV log-sum-exp merge, "The Rescaling and Online Softmax Reduction
+// Algorithm"): L = log2 sum_s 2^L_s, O = sum_s 2^(L_s - L) O_s. `first_phase`: the piece
+// belongs to the step's first pass, which records flags, statistics and the flagged list.
 template <typename T, int D, int G>
-__device__ __forceinline__ void combine_piece(const Params& p, const Piece& pc, float* mm,
-                                              float* ml, uint32_t* mflag, float* wbuf, int* misc,
-                                              int warp, int lane, int ctid) {
+__device__ __forceinline__ void combine_piece(const Params& p, const Piece& pc, bool first_phase,
+                                              float* mm, float* ml, uint32_t* mflag,
+                                              float* wbuf, int* misc, int warp, int lane,
+                                              int ctid) {
   constexpr int kCT = kConsumerWarps * 32;
   constexpr float kLn2 = 0.6931471805599453f;
   constexpr int W = warp_scratch_floats(D, G, (int)sizeof(T));
@@ -583,14 +588,14 @@ __device__ __forceinline__ void combine_piece(const Params& p, const Piece& pc, 
       store_out(p.out, (row0 + g) * D + d, p.out_dtype, o);
       if (d == 0) {
         if (p.out_lse) p.out_lse[row0 + g] = L2 * kLn2;
-        if (p.row_flags && p.write_flags) p.row_flags[row0 + g] = (uint8_t)((fl >> g) & 1u);
+        if (p.row_flags && first_phase) p.row_flags[row0 + g] = (uint8_t)((fl >> g) & 1u);
       }
     } else {
       __stcg(p.part_o + ((long long)pc.slot * G + g) * D + d, o);
       if (d == 0) __stcg(p.part_l + (long long)pc.slot * G + g, L2);
     }
   }
-  if (ctid == 0 && p.write_flags && fl) {
+  if (ctid == 0 && first_phase && fl) {
     atomicAdd(p.stats + 1, (unsigned long long)__popc(fl));
     if (direct) {
       atomicAdd(p.stats + 0, (unsigned long long)__popc(fl));
@@ -599,13 +604,8 @@ __device__ __forceinline__ void combine_piece(const Params& p, const Piece& pc, 
     }
   }
 
-  if (!p.inline_merge && ctid == 0 && pc.slot == pc.slot_base)
-    p.desc[pc.g] = make_int2(pc.slot_base, direct ? 1 : pc.nslots);   // for the merge kernel
-
   if (!direct) {
     if (ctid == 0) __stcg(p.part_flags + pc.slot, fl);
-  }
-  if (!direct && p.inline_merge) {
     __threadfence();
     named_bar_sync(1, kCT);
     if (ctid == 0) {
@@ -615,13 +615,26 @@ __device__ __forceinline__ void combine_piece(const Params& p, const Piece& pc, 
     }
     named_bar_sync(1, kCT);
     if (misc[0]) {
-      // Last piece of the group: exact log-sum-exp merge of all its partials. Every pass is
-      // parallel over slots so the merge pays the L2 latency a few times, not per slot.
+      // Last piece of the group: merge all its partials. Each pass issues all of its loads
+      // before using any, so the merge pays the L2 latency a few times, not per piece.
       __threadfence();
       const int S = pc.nslots;
       float* wts = wbuf;              // [S, G] weights (scratch reused; S <= 8 * D)
       float* hsum = mm;               // [G] sum of weights
       float* hmax = ml;               // [G] maximum partial LSE
+      // O = sum_s w_s O_s / sum_s w_s: each thread owns EPT elements and keeps 32 partial
+      // loads in flight per block of pieces; the first block is loaded with the LSEs
+      constexpr int EPT = (G * D + kCT - 1) / kCT;
+      constexpr int SB = 32 / EPT;
+      const float* po = p.part_o + (long long)pc.slot_base * G * D;
+      float o[EPT][SB];
+#pragma unroll
+      for (int i = 0; i < EPT; ++i) {
+        const int e = ctid + i * kCT;
+#pragma unroll
+        for (int j = 0; j < SB; ++j)
+          o[i][j] = (e < G * D && j < S) ? __ldcg(po + (long long)j * G * D + e) : 0.f;
+      }
       const float* pl = p.part_l + (long long)pc.slot_base * G;
       for (int i = ctid; i < S * G; i += kCT) wts[i] = __ldcg(pl + i);
       uint32_t rf = 0;
@@ -650,33 +663,46 @@ __device__ __forceinline__ void combine_piece(const Params& p, const Piece& pc, 
         }
       }
       named_bar_sync(1, kCT);
-      const float* po = p.part_o + (long long)pc.slot_base * G * D;
-      for (int e = ctid; e < G * D; e += kCT) {
-        const int g = e / D, d = e - (e / D) * D;
-        float num = 0.f;
-        int s = 0;
-        for (; s + 4 <= S; s += 4) {
-          const float o0 = __ldcg(po + (long long)(s + 0) * G * D + e);
-          const float o1 = __ldcg(po + (long long)(s + 1) * G * D + e);
-          const float o2 = __ldcg(po + (long long)(s + 2) * G * D + e);
-          const float o3 = __ldcg(po + (long long)(s + 3) * G * D + e);
-          num += wts[(s + 0) * G + g] * o0 + wts[(s + 1) * G + g] * o1 +
-                 wts[(s + 2) * G + g] * o2 + wts[(s + 3) * G + g] * o3;
+      float num[EPT];
+#pragma unroll
+      for (int i = 0; i < EPT; ++i) num[i] = 0.f;
+      for (int s0 = 0; s0 < S; s0 += SB) {
+        if (s0 > 0) {
+#pragma unroll
+          for (int i = 0; i < EPT; ++i) {
+            const int e = ctid + i * kCT;
+#pragma unroll
+            for (int j = 0; j < SB; ++j)
+              o[i][j] = (e < G * D && s0 + j < S)
+                            ? __ldcg(po + (long long)(s0 + j) * G * D + e) : 0.f;
+          }
         }
-        for (; s < S; ++s) num += wts[s * G + g] * __ldcg(po + (long long)s * G * D + e);
-        const float sum = hsum[g];
-        const float o = sum > 0.f ? num / sum : 0.f;
-        store_out(p.out, (row0 + g) * D + d, p.out_dtype, o);
-        if (d == 0) {
-          if (p.out_lse) p.out_lse[row0 + g] = sum > 0.f ? (hmax[g] + fast_log2(sum)) * kLn2 : -INFINITY;
-          if (p.row_flags && p.write_flags)
-            p.row_flags[row0 + g] = (uint8_t)((((uint32_t)misc[1]) >> g) & 1u);
+#pragma unroll
+        for (int i = 0; i < EPT; ++i) {
+          const int g = min(ctid + i * kCT, G * D - 1) / D;
+#pragma unroll
+          for (int j = 0; j < SB; ++j)
+            if (s0 + j < S) num[i] += wts[(s0 + j) * G + g] * o[i][j];
+        }
+      }
+      const uint32_t rfa = (uint32_t)misc[1];
+#pragma unroll
+      for (int i = 0; i < EPT; ++i) {
+        const int e = ctid + i * kCT;
+        if (e < G * D) {
+          const int g = e / D, d = e - (e / D) * D;
+          const float sum = hsum[g];
+          store_out(p.out, (row0 + g) * D + d, p.out_dtype, sum > 0.f ? num[i] / sum : 0.f);
+          if (d == 0) {
+            if (p.out_lse)
+              p.out_lse[row0 + g] = sum > 0.f ? (hmax[g] + fast_log2(sum)) * kLn2 : -INFINITY;
+            if (p.row_flags && first_phase) p.row_flags[row0 + g] = (uint8_t)((rfa >> g) & 1u);
+          }
         }
       }
       if (ctid == 0) {
         p.counters[pc.g] = 0;   // leave the counter ready for the next run
-        const uint32_t rfa = (uint32_t)misc[1];
-        if (p.write_flags && rfa) {
+        if (first_phase && rfa) {
           atomicAdd(p.stats + 0, (unsigned long long)__popc(rfa));
           const int at = atomicAdd(p.list_state, 1);
           if (at < p.n_groups) p.flag_list[at] = pc.g;
@@ -690,7 +716,8 @@ __device__ __forceinline__ void combine_piece(const Params& p, const Piece& pc, 
 template <typename T, int D, int G, bool UNIFIED>
 __device__ __forceinline__ void run_consumers(const Params& p, Sched s, uint8_t* stages,
                                               const Layout& L, uint64_t* full, uint64_t* empty,
-                                              uint8_t* smem, int warp, int lane) {
+                                              uint8_t* smem, int warp, int lane, uint32_t& k,
+                                              bool& dead) {
   using C = Cfg<T, D, G>;
   constexpr int E = C::kEpl;
   const uint32_t NS = (uint32_t)p.stages;
@@ -702,8 +729,6 @@ __device__ __forceinline__ void run_consumers(const Params& p, Sched s, uint8_t*
   int* misc = reinterpret_cast<int*>(smem + L.misc_off);
   const LaneMap<T, D, G> lm(warp, lane);
   const int ctid = warp * 32 + lane;
-  uint32_t k = 0;
-  bool dead = false;
   Piece pc;
   constexpr int E2 = E / 2;
   while (sched_next(s, p, pc)) {
@@ -766,7 +791,7 @@ __device__ __forceinline__ void run_consumers(const Params& p, Sched s, uint8_t*
 #pragma unroll
       for (int e = 0; e < E2; ++e) f2_unpack(acc2[g][e], acc[g][2 * e], acc[g][2 * e + 1]);
     publish_cuda<T, D, G>(lm, acc, dl, m, fmask, mm, ml, mflag, wbuf, warp, lane);
-    combine_piece<T, D, G>(p, pc, mm, ml, mflag, wbuf, misc, warp, lane, ctid);
+    combine_piece<T, D, G>(p, pc, s.first_phase, mm, ml, mflag, wbuf, misc, warp, lane, ctid);
   }
 }
 
@@ -776,7 +801,7 @@ template <typename T, int D, int G, bool UNIFIED>
 __device__ __forceinline__ void run_consumers_mma(const Params& p, Sched s, uint8_t* stages,
                                                   const Layout& L, uint64_t* full,
                                                   uint64_t* empty, uint8_t* smem, int warp,
-                                                  int lane) {
+                                                  int lane, uint32_t& k, bool& dead) {
   const uint32_t NS = (uint32_t)p.stages;
   float* wbuf = reinterpret_cast<float*>(smem + L.wbuf_off);
   float* mm = reinterpret_cast<float*>(smem + L.mm_off);
@@ -785,8 +810,6 @@ __device__ __forceinline__ void run_consumers_mma(const Params& p, Sched s, uint
   int* misc = reinterpret_cast<int*>(smem + L.misc_off);
   const int ctid = warp * 32 + lane;
   const int row0 = warp * kTokensPerWarp;
-  uint32_t k = 0;
-  bool dead = false;
   Piece pc;
   while (sched_next(s, p, pc)) {
     MmaState<D, G> st;
@@ -826,10 +849,46 @@ __device__ __forceinline__ void run_consumers_mma(const Params& p, Sched s, uint
       k += pair ? 2u : 1u;
     }
     publish_mma<T, D, G>(st, UNIFIED ? p.phi2 : st.m, fmask, mm, ml, mflag, wbuf, warp, lane);
-    combine_piece<T, D, G>(p, pc, mm, ml, mflag, wbuf, misc, warp, lane, ctid);
+    combine_piece<T, D, G>(p, pc, s.first_phase, mm, ml, mflag, wbuf, misc, warp, lane, ctid);
   }
 }
 
+// A consumer warp's role over the launch's pieces.
+template <typename T, int D, int G, bool UNIFIED>
+__device__ __forceinline__ void consumer_role(const Params& p, const Sched& s, uint8_t* smem,
+                                              const Layout& L, uint64_t* full, uint64_t* empty,
+                                              int warp, int lane) {
+  constexpr bool kMma = uses_mma(sizeof(T), std::is_same<T, __nv_bfloat16>::value, G);
+  uint32_t k = 0;
+  bool dead = false;
+  if constexpr (kMma)
+    run_consumers_mma<T, D, G, UNIFIED>(p, s, smem, L, full, empty, smem, warp, lane, k, dead);
+  else
+    run_consumers<T, D, G, UNIFIED>(p, s, smem, L, full, empty, smem, warp, lane, k, dead);
+}
+
+// A producer-warpgroup warp's role (two warps issue copies for a contiguous cache, four for a
+// paged one; the others have nothing to do).
+template <typename T, int D, int G>
+__device__ __forceinline__ void producer_role(const Params& p, const Sched& s, uint8_t* smem,
+                                              const Layout& L, uint64_t* full, uint64_t* empty,
+                                              const CUtensorMap* tmk, const CUtensorMap* tmv,
+                                              int warp, int lane) {
+  constexpr bool kMma = uses_mma(sizeof(T), std::is_same<T, __nv_bfloat16>::value, G);
+  uint32_t k = 0;
+  bool dead = false;
+  if (warp < kConsumerWarps + (p.paged ? 4 : 2))
+    run_producer<T, D, G, kMma>(p, s, smem, L, full, empty, tmk, tmv, lane,
+                                warp - kConsumerWarps, k, dead);
+}
+
+// The split kernel. A step's first launch computes every group with the step's softmax mode
+// (balanced shares, or uniform splits of every group); the last piece of each group to finish
+// merges the group. In unified mode a second launch of the synchronised kernel follows as a
+// programmatic dependent (`recompute`): it waits for the first launch's results, reads the
+// list of groups whose range check failed and recomputes them with the synchronised softmax
+// as uniform splits ("The Overflow Fallback: Recomputation"); with nothing flagged it exits
+// at once.
 template <typename T, int D, int G, bool UNIFIED>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_split_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmk,
@@ -844,6 +903,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* lens = reinterpret_cast<int*>(smem + L.lens_off);
   int* prefix = reinterpret_cast<int*>(smem + L.prefix_off);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int nflagged = 0;
+  if (p.recompute) {
+    // the first launch's flagged list is complete and visible after this wait; with nothing
+    // flagged the recompute launch has no work (and nothing to reset)
+    pdl_wait();
+    nflagged = min(__ldcg(p.list_state), p.n_groups);
+    if (nflagged == 0) return;
+  }
 
   if (tid == 0) {
     for (int s = 0; s < p.stages; ++s) {
@@ -856,9 +923,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&tmk);
     prefetch_tensormap(&tmv);
   }
-  // Inputs written by a predecessor launched with programmatic serialization (and, for
-  // the recompute pass, the flagged-group list) are visible after this point.
-  pdl_wait();
 
   Sched s;
   s.policy = p.policy;
@@ -869,7 +933,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   s.u = s.u1 = s.W = 0;
   s.i = s.i1 = 0;
   s.S = p.num_splits > 0 ? p.num_splits : 1;
-  if (p.policy == kBalanced) {
+  s.use_list = p.recompute != 0;
+  s.first_phase = p.recompute == 0;
+  if (p.recompute) {
+    const long long ni = (long long)nflagged * s.S;
+    s.i = (long long)blockIdx.x * ni / gridDim.x;
+    s.i1 = ((long long)blockIdx.x + 1) * ni / gridDim.x;
+  } else if (p.policy == kBalanced) {
     for (int b = tid; b < p.batch; b += blockDim.x) {
       const int raw = __ldg(p.seq_lens + b);
       const int n = clamp_len(p, raw);
@@ -913,45 +983,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int e = tid; e < p.hq * D; e += blockDim.x) store_out(p.out, r0 * D + e, p.out_dtype, 0.f);
       for (int h = tid; h < p.hq; h += blockDim.x) {
         if (p.out_lse) p.out_lse[r0 + h] = -INFINITY;
-        if (p.row_flags && p.write_flags) p.row_flags[r0 + h] = 0;
+        if (p.row_flags) p.row_flags[r0 + h] = 0;
       }
-      for (int kv = tid; kv < p.hkv; kv += blockDim.x)
-        if (!p.inline_merge) p.desc[(long long)b * p.hkv + kv] = make_int2(0, 0);
     }
   } else {
-    long long groups = p.n_groups;
-    if (p.use_list) {
-      const int nf = min(__ldcg(p.list_state), p.n_groups);
-      if (nf <= 0) return;   // nothing was flagged: the recompute pass has no work
-      groups = nf;
-    }
-    const long long ni = groups * s.S;
+    const long long ni = (long long)p.n_groups * s.S;
     s.i = (long long)blockIdx.x * ni / gridDim.x;
     s.i1 = ((long long)blockIdx.x + 1) * ni / gridDim.x;
   }
   __syncthreads();
-  pdl_launch_dependents();
+  // a dependent launch (the recompute) may start its launch while this grid runs
+  if (!p.recompute) pdl_launch_dependents();
 
-  uint8_t* stages = smem;
-  // Registers move from the producer warpgroup (one working warp) to the two consumer
-  // warpgroups: 8 * 32 * kConsumerRegs + 4 * 32 * kProducerRegs equals the launch's
+  // Registers move from the producer warpgroup (two or four working warps) to the two
+  // consumer warpgroups: 8 * 32 * kConsumerRegs + 4 * 32 * kProducerRegs equals the launch's
   // 12 * 32 * 168 (checked on the host before the first launch).
-  constexpr bool kMma = uses_mma(sizeof(T), std::is_same<T, __nv_bfloat16>::value, G);
   if (warp < kConsumerWarps) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
-    if constexpr (kMma)
-      run_consumers_mma<T, D, G, UNIFIED>(p, s, stages, L, full, empty, smem, warp, lane);
-    else
-      run_consumers<T, D, G, UNIFIED>(p, s, stages, L, full, empty, smem, warp, lane);
+    consumer_role<T, D, G, UNIFIED>(p, s, smem, L, full, empty, warp, lane);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
-    if (warp < kConsumerWarps + (p.paged ? 4 : 2))
-      run_producer<T, D, G, kMma>(p, s, stages, L, full, empty, &tmk, &tmv, lane,
-                                  warp - kConsumerWarps);
+    producer_role<T, D, G>(p, s, smem, L, full, empty, &tmk, &tmv, warp, lane);
   }
 
-  if (p.use_list) {
-    // the recompute pass's last CTA resets the flagged list for the next run
+  if (p.recompute) {
+    // the recompute launch's last CTA resets the flagged list for the next step
     __syncthreads();
     if (tid == 0) {
       __threadfence();

@@ -161,8 +161,7 @@ __device__ __forceinline__ void mma_consume(const Params& p, MmaState<D, G>& st,
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       pr[b][e] = valid[b][e] ? fast_exp2(x[b][e] - ref) : 0.f;
-      if constexpr (UNIFIED)
-        if (valid[b][e] && (x[b][e] < p.lo2 || x[b][e] > p.hi2)) fmask |= 1u << head;
+      if (UNIFIED && valid[b][e] && (x[b][e] < p.lo2 || x[b][e] > p.hi2)) fmask |= 1u << head;
       st.den += pr[b][e];
     }
   // P as A fragments (k = token: stage 0 rows in k 0..7, stage 1 rows in k 8..15), hi + lo
