@@ -72,6 +72,15 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
+// Grid for `items` equal uniform-split items: the fewest CTAs that still give every CTA the
+// smallest possible number of items (512 items on 152 SMs: 128 CTAs of 4 rather than a mix
+// of 3 and 4, whose slowest CTAs would set the step time).
+int uniform_grid(long long items, int sms) {
+  if (items <= 0) return 1;
+  const long long per = (items + sms - 1) / sms;
+  return (int)((items + per - 1) / per);
+}
+
 int elem_size(int dt) { return dt == DA_F32 ? 4 : 2; }
 
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
@@ -320,7 +329,7 @@ int decode_attn_plan(const da_problem* problem, int num_splits, da_plan** plan_o
   const long long min_ctas = (w_max + kMinUnitsPerCta - 1) / kMinUnitsPerCta;
   pl->grid = pl->policy == kBalanced
                  ? (int)std::max<long long>(1, std::min<long long>(sms, min_ctas))
-                 : (int)std::min<long long>(sms, (long long)pl->n_groups * pl->num_splits);
+                 : uniform_grid((long long)pl->n_groups * pl->num_splits, sms);
   pl->recompute_splits = (int)std::min<long long>(
       units_max, std::max(1, (sms + pl->n_groups - 1) / pl->n_groups));
   const long long need_uniform =
@@ -481,7 +490,7 @@ int decode_attn_run_ex(const da_plan* plan, const da_run_args* args) {
   kp.hi2 = (float)(((double)p.unified_max + p.range_hi) * log2e);
   const int grid = policy == kBalanced
                        ? pl.grid
-                       : (int)std::min<long long>(pl.num_sms, (long long)pl.n_groups * S);
+                       : uniform_grid((long long)pl.n_groups * S, pl.num_sms);
 
   const bool sync_after = stats != nullptr || p.validate;
   char* ws = static_cast<char*>(workspace);
@@ -528,8 +537,8 @@ int decode_attn_run_ex(const da_plan* plan, const da_run_args* args) {
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t rcfg = cfg;
-    rcfg.gridDim = dim3((unsigned)std::min<long long>(
-        pl.num_sms, (long long)pl.n_groups * pl.recompute_splits));
+    rcfg.gridDim = dim3((unsigned)uniform_grid((long long)pl.n_groups * pl.recompute_splits,
+                                                pl.num_sms));
     rcfg.attrs = pdl;
     rcfg.numAttrs = 1;
     void* rargs[3] = {&rp, &tmk, &tmv};   // same consumer kind, same tile layout

@@ -853,12 +853,60 @@ __device__ __forceinline__ void run_consumers_mma(const Params& p, Sched s, uint
   }
 }
 
+// The dynamic shared memory, aligned to 1024 bytes (the 128-byte swizzle's period).
+__device__ __forceinline__ uint8_t* smem_base() {
+  extern __shared__ uint8_t smem_raw[];
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                    ~static_cast<uintptr_t>(1023));
+}
+
+// The launch's schedule for this CTA, from the parameters and what the prologue left in shared
+// memory (lengths and prefix for balanced shares, the flagged count for a recompute launch).
+// The roles rebuild it after the register split, so that nothing but the parameters stays live
+// across it: the producer warps' small register budget then holds only their own state.
+__device__ __forceinline__ Sched launch_sched(const Params& p, const int* lens, const int* prefix,
+                                              const int* misc) {
+  Sched s;
+  s.policy = p.policy;
+  s.P = gridDim.x;
+  s.c = blockIdx.x;
+  s.lens = lens;
+  s.prefix = prefix;
+  s.u = s.u1 = s.W = 0;
+  s.i = s.i1 = 0;
+  s.S = p.num_splits > 0 ? p.num_splits : 1;
+  s.use_list = p.recompute != 0;
+  s.first_phase = p.recompute == 0;
+  if (p.recompute || p.policy != kBalanced) {
+    const long long ni = (long long)(p.recompute ? misc[2] : p.n_groups) * s.S;
+    s.i = (long long)blockIdx.x * ni / gridDim.x;
+    s.i1 = ((long long)blockIdx.x + 1) * ni / gridDim.x;
+  } else {
+    s.W = (long long)p.hkv * prefix[p.batch];
+    // The grid is sized from the cache capacity; when the step holds fewer units than CTAs,
+    // only the first W CTAs take shares, so that every share is non-empty and a group's
+    // pieces sit on consecutive CTAs (its piece count is then cl - cf + 1).
+    s.P = (int)(s.W < (long long)gridDim.x ? s.W : (long long)gridDim.x);
+    if ((int)blockIdx.x < s.P) {
+      s.u = (long long)blockIdx.x * s.W / s.P;
+      s.u1 = ((long long)blockIdx.x + 1) * s.W / s.P;
+    }
+  }
+  return s;
+}
+
 // A consumer warp's role over the launch's pieces.
 template <typename T, int D, int G, bool UNIFIED>
-__device__ __forceinline__ void consumer_role(const Params& p, const Sched& s, uint8_t* smem,
-                                              const Layout& L, uint64_t* full, uint64_t* empty,
-                                              int warp, int lane) {
+__device__ __forceinline__ void consumer_role(const Params& p, int warp, int lane) {
+  using C = Cfg<T, D, G>;
   constexpr bool kMma = uses_mma(sizeof(T), std::is_same<T, __nv_bfloat16>::value, G);
+  uint8_t* smem = smem_base();
+  const Layout L = make_layout(D, G, C::kEs, p.stages, p.batch_smem);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
+  uint64_t* empty = full + p.stages;
+  const Sched s = launch_sched(p, reinterpret_cast<const int*>(smem + L.lens_off),
+                               reinterpret_cast<const int*>(smem + L.prefix_off),
+                               reinterpret_cast<const int*>(smem + L.misc_off));
   uint32_t k = 0;
   bool dead = false;
   if constexpr (kMma)
@@ -870,16 +918,22 @@ __device__ __forceinline__ void consumer_role(const Params& p, const Sched& s, u
 // A producer-warpgroup warp's role (two warps issue copies for a contiguous cache, four for a
 // paged one; the others have nothing to do).
 template <typename T, int D, int G>
-__device__ __forceinline__ void producer_role(const Params& p, const Sched& s, uint8_t* smem,
-                                              const Layout& L, uint64_t* full, uint64_t* empty,
-                                              const CUtensorMap* tmk, const CUtensorMap* tmv,
-                                              int warp, int lane) {
+__device__ __forceinline__ void producer_role(const Params& p, const CUtensorMap* tmk,
+                                              const CUtensorMap* tmv, int warp, int lane) {
+  using C = Cfg<T, D, G>;
   constexpr bool kMma = uses_mma(sizeof(T), std::is_same<T, __nv_bfloat16>::value, G);
+  if (warp >= kConsumerWarps + (p.paged ? 4 : 2)) return;
+  uint8_t* smem = smem_base();
+  const Layout L = make_layout(D, G, C::kEs, p.stages, p.batch_smem);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
+  uint64_t* empty = full + p.stages;
+  const Sched s = launch_sched(p, reinterpret_cast<const int*>(smem + L.lens_off),
+                               reinterpret_cast<const int*>(smem + L.prefix_off),
+                               reinterpret_cast<const int*>(smem + L.misc_off));
   uint32_t k = 0;
   bool dead = false;
-  if (warp < kConsumerWarps + (p.paged ? 4 : 2))
-    run_producer<T, D, G, kMma>(p, s, smem, L, full, empty, tmk, tmv, lane,
-                                warp - kConsumerWarps, k, dead);
+  run_producer<T, D, G, kMma>(p, s, smem, L, full, empty, tmk, tmv, lane, warp - kConsumerWarps,
+                              k, dead);
 }
 
 // The split kernel. A step's first launch computes every group with the step's softmax mode
@@ -894,104 +948,74 @@ __global__ void __launch_bounds__(kThreads, 1)
     decode_split_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv) {
   using C = Cfg<T, D, G>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  const Layout L = make_layout(D, G, C::kEs, p.stages, p.batch_smem);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
-  uint64_t* empty = full + p.stages;
-  int* lens = reinterpret_cast<int*>(smem + L.lens_off);
-  int* prefix = reinterpret_cast<int*>(smem + L.prefix_off);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  int nflagged = 0;
   if (p.recompute) {
     // the first launch's flagged list is complete and visible after this wait; with nothing
     // flagged the recompute launch has no work (and nothing to reset)
     pdl_wait();
-    nflagged = min(__ldcg(p.list_state), p.n_groups);
-    if (nflagged == 0) return;
+    if (min(__ldcg(p.list_state), p.n_groups) == 0) return;
   }
-
-  if (tid == 0) {
-    for (int s = 0; s < p.stages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
+  {
+    uint8_t* smem = smem_base();
+    const Layout L = make_layout(D, G, C::kEs, p.stages, p.batch_smem);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
+    uint64_t* empty = full + p.stages;
+    int* lens = reinterpret_cast<int*>(smem + L.lens_off);
+    int* prefix = reinterpret_cast<int*>(smem + L.prefix_off);
+    int* misc = reinterpret_cast<int*>(smem + L.misc_off);
+    if (tid == 0) {
+      for (int s = 0; s < p.stages; ++s) {
+        mbar_init(&full[s], 1);
+        mbar_init(&empty[s], kConsumerWarps);
+      }
+      fence_mbar_init();
+      if (p.recompute) misc[2] = min(__ldcg(p.list_state), p.n_groups);
     }
-    fence_mbar_init();
-  }
-  if (warp == kConsumerWarps && lane == 0) {
-    prefetch_tensormap(&tmk);
-    prefetch_tensormap(&tmv);
-  }
-
-  Sched s;
-  s.policy = p.policy;
-  s.P = gridDim.x;
-  s.c = blockIdx.x;
-  s.lens = lens;
-  s.prefix = prefix;
-  s.u = s.u1 = s.W = 0;
-  s.i = s.i1 = 0;
-  s.S = p.num_splits > 0 ? p.num_splits : 1;
-  s.use_list = p.recompute != 0;
-  s.first_phase = p.recompute == 0;
-  if (p.recompute) {
-    const long long ni = (long long)nflagged * s.S;
-    s.i = (long long)blockIdx.x * ni / gridDim.x;
-    s.i1 = ((long long)blockIdx.x + 1) * ni / gridDim.x;
-  } else if (p.policy == kBalanced) {
-    for (int b = tid; b < p.batch; b += blockDim.x) {
-      const int raw = __ldg(p.seq_lens + b);
-      const int n = clamp_len(p, raw);
-      if (n != raw && blockIdx.x == 0) atomicOr(p.status, kStatusBadSeqLen);
-      lens[b] = n;
+    if (warp == kConsumerWarps && lane == 0) {
+      prefetch_tensormap(&tmk);
+      prefetch_tensormap(&tmv);
     }
-    __syncthreads();
-    if (warp == 0) {
-      const int per = (p.batch + 31) / 32;
-      const int beg = min(p.batch, lane * per), end = min(p.batch, beg + per);
-      int local = 0;
-      for (int b = beg; b < end; ++b)
-        local += lens[b] ? (lens[b] + p.unit - 1) / p.unit + p.piece_units : 0;
-      int incl = local;
+    if (!p.recompute && p.policy == kBalanced) {
+      for (int b = tid; b < p.batch; b += blockDim.x) {
+        const int raw = __ldg(p.seq_lens + b);
+        const int n = clamp_len(p, raw);
+        if (n != raw && blockIdx.x == 0) atomicOr(p.status, kStatusBadSeqLen);
+        lens[b] = n;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        const int per = (p.batch + 31) / 32;
+        const int beg = min(p.batch, lane * per), end = min(p.batch, beg + per);
+        int local = 0;
+        for (int b = beg; b < end; ++b)
+          local += lens[b] ? (lens[b] + p.unit - 1) / p.unit + p.piece_units : 0;
+        int incl = local;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        int run = incl - local;
+        for (int b = beg; b < end; ++b) {
+          prefix[b] = run;
+          run += lens[b] ? (lens[b] + p.unit - 1) / p.unit + p.piece_units : 0;
+        }
+        if (lane == 31) prefix[p.batch] = incl;
       }
-      int run = incl - local;
-      for (int b = beg; b < end; ++b) {
-        prefix[b] = run;
-        run += lens[b] ? (lens[b] + p.unit - 1) / p.unit + p.piece_units : 0;
+      // sequences with no tokens have no piece: out = 0, lse = -inf, flag = 0
+      for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
+        if (lens[b] != 0) continue;
+        const long long r0 = (long long)b * p.hq;
+        for (int e = tid; e < p.hq * D; e += blockDim.x)
+          store_out(p.out, r0 * D + e, p.out_dtype, 0.f);
+        for (int h = tid; h < p.hq; h += blockDim.x) {
+          if (p.out_lse) p.out_lse[r0 + h] = -INFINITY;
+          if (p.row_flags) p.row_flags[r0 + h] = 0;
+        }
       }
-      if (lane == 31) prefix[p.batch] = incl;
     }
     __syncthreads();
-    s.W = (long long)p.hkv * prefix[p.batch];
-    // The grid is sized from the cache capacity; when the step holds fewer units than CTAs,
-    // only the first W CTAs take shares, so that every share is non-empty and a group's
-    // pieces sit on consecutive CTAs (its piece count is then cl - cf + 1).
-    s.P = (int)(s.W < (long long)gridDim.x ? s.W : (long long)gridDim.x);
-    if ((int)blockIdx.x < s.P) {
-      s.u = (long long)blockIdx.x * s.W / s.P;
-      s.u1 = ((long long)blockIdx.x + 1) * s.W / s.P;
-    }
-    // sequences with no tokens have no piece: out = 0, lse = -inf, flag = 0
-    for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
-      if (lens[b] != 0) continue;
-      const long long r0 = (long long)b * p.hq;
-      for (int e = tid; e < p.hq * D; e += blockDim.x) store_out(p.out, r0 * D + e, p.out_dtype, 0.f);
-      for (int h = tid; h < p.hq; h += blockDim.x) {
-        if (p.out_lse) p.out_lse[r0 + h] = -INFINITY;
-        if (p.row_flags) p.row_flags[r0 + h] = 0;
-      }
-    }
-  } else {
-    const long long ni = (long long)p.n_groups * s.S;
-    s.i = (long long)blockIdx.x * ni / gridDim.x;
-    s.i1 = ((long long)blockIdx.x + 1) * ni / gridDim.x;
   }
-  __syncthreads();
   // a dependent launch (the recompute) may start its launch while this grid runs
   if (!p.recompute) pdl_launch_dependents();
 
@@ -1000,10 +1024,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // 12 * 32 * 168 (checked on the host before the first launch).
   if (warp < kConsumerWarps) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
-    consumer_role<T, D, G, UNIFIED>(p, s, smem, L, full, empty, warp, lane);
+    consumer_role<T, D, G, UNIFIED>(p, warp, lane);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
-    producer_role<T, D, G>(p, s, smem, L, full, empty, &tmk, &tmv, warp, lane);
+    producer_role<T, D, G>(p, &tmk, &tmv, warp, lane);
   }
 
   if (p.recompute) {
