@@ -519,26 +519,42 @@ __device__ __forceinline__ void publish_cuda(const LaneMap<T, D, G>& lm,
   }
 }
 
-// Publish a tensor-core warp's piece state (same scratch format as publish_cuda).
+// Publish a tensor-core warp's piece state (same scratch format as publish_cuda): the lane
+// holds O^T elements (d = 16 mt + lane / 4 and d + 8) of heads hp = 2 (lane % 4) and hp + 1,
+// and its share of those heads' denominators; the 8 lanes sharing lane % 4 complete a head.
 template <typename T, int D, int G>
-__device__ __forceinline__ void publish_mma(const MmaState<D, G>& st, float m, uint32_t fmask,
-                                            float* mm, float* ml, uint32_t* mflag, float* wbuf,
-                                            int warp, int lane) {
+__device__ __forceinline__ void publish_mma(const MmaState<D, G>& st, float m0, float m1,
+                                            uint32_t fmask, float* mm, float* ml,
+                                            uint32_t* mflag, float* wbuf, int warp, int lane) {
   constexpr int W = warp_scratch_floats(D, G, (int)sizeof(T));
-  const int head = lane >> 2, c0 = 2 * (lane & 3);
-  float den = st.den;
-  den += __shfl_xor_sync(0xffffffffu, den, 1);
-  den += __shfl_xor_sync(0xffffffffu, den, 2);
-  const uint32_t fm = __reduce_or_sync(0xffffffffu, fmask);
-  if (head < G) {
+  const int hp = 2 * (lane & 3), dr = lane >> 2;
+  float den0 = st.den[0], den1 = st.den[1];
 #pragma unroll
-    for (int j = 0; j < D / 8; ++j) {
-      wbuf[warp * W + head * D + 8 * j + c0] = st.o[j][0];
-      wbuf[warp * W + head * D + 8 * j + c0 + 1] = st.o[j][1];
+  for (int o = 4; o <= 16; o <<= 1) {
+    den0 += __shfl_xor_sync(0xffffffffu, den0, o);
+    den1 += __shfl_xor_sync(0xffffffffu, den1, o);
+  }
+  const uint32_t fm = __reduce_or_sync(0xffffffffu, fmask);
+  float* w0 = wbuf + warp * W + hp * D + dr;
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt) {
+    if (hp < G) {
+      w0[mt * 16] = st.o[mt][0];
+      w0[mt * 16 + 8] = st.o[mt][2];
     }
-    if ((lane & 3) == 0) {
-      mm[warp * G + head] = m;
-      ml[warp * G + head] = den;
+    if (hp + 1 < G) {
+      w0[D + mt * 16] = st.o[mt][1];
+      w0[D + mt * 16 + 8] = st.o[mt][3];
+    }
+  }
+  if (lane < 4) {
+    if (hp < G) {
+      mm[warp * G + hp] = m0;
+      ml[warp * G + hp] = den0;
+    }
+    if (hp + 1 < G) {
+      mm[warp * G + hp + 1] = m1;
+      ml[warp * G + hp + 1] = den1;
     }
   }
   if (lane == 0) mflag[warp] = fm;
@@ -810,15 +826,16 @@ __device__ __forceinline__ void run_consumers_mma(const Params& p, Sched s, uint
   int* misc = reinterpret_cast<int*>(smem + L.misc_off);
   const int ctid = warp * 32 + lane;
   const int row0 = warp * kTokensPerWarp;
+  const MmaLane<D> mlane(row0, lane);
   Piece pc;
   while (sched_next(s, p, pc)) {
     MmaState<D, G> st;
 #pragma unroll
-    for (int j = 0; j < D / 8; ++j)
+    for (int j = 0; j < D / 16; ++j)
 #pragma unroll
       for (int i = 0; i < 4; ++i) st.o[j][i] = 0.f;
-    st.den = 0.f;
-    st.m = -INFINITY;
+    st.den[0] = st.den[1] = 0.f;
+    st.m[0] = st.m[1] = -INFINITY;
     uint32_t fmask = 0;
     const int nst = (pc.t1 - pc.t0 + kStageTokens - 1) / kStageTokens;
     for (int j = 0; j < nst; j += 2) {
@@ -838,9 +855,10 @@ __device__ __forceinline__ void run_consumers_mma(const Params& p, Sched s, uint
       const int ts = pc.t0 + j * kStageTokens;
       const int n[2] = {min(kStageTokens, pc.t1 - ts),
                         pair ? min(kStageTokens, pc.t1 - ts - kStageTokens) : 0};
-      const uint8_t* const kss[2] = {st0 + L.k_off, st1 + L.k_off};
-      const uint8_t* const vss[2] = {st0 + L.v_off, st1 + L.v_off};
-      if (!dead) mma_consume<D, G, UNIFIED>(p, st, kss, vss, n, row0, lane, fmask);
+      const uint8_t* const st1m = pair ? st1 : st0;   // no second stage: read stage 0 again
+      const uint32_t kt[2] = {smem_u32(st0 + L.k_off), smem_u32(st1m + L.k_off)};
+      const uint32_t vt[2] = {smem_u32(st0 + L.v_off), smem_u32(st1m + L.v_off)};
+      if (!dead) mma_consume<D, G, UNIFIED>(p, st, mlane, kt, vt, n, row0, lane, fmask);
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&empty[s0]);
@@ -848,7 +866,8 @@ __device__ __forceinline__ void run_consumers_mma(const Params& p, Sched s, uint
       }
       k += pair ? 2u : 1u;
     }
-    publish_mma<T, D, G>(st, UNIFIED ? p.phi2 : st.m, fmask, mm, ml, mflag, wbuf, warp, lane);
+    publish_mma<T, D, G>(st, UNIFIED ? p.phi2 : st.m[0], UNIFIED ? p.phi2 : st.m[1], fmask, mm,
+                         ml, mflag, wbuf, warp, lane);
     combine_piece<T, D, G>(p, pc, s.first_phase, mm, ml, mflag, wbuf, misc, warp, lane, ctid);
   }
 }

@@ -1,15 +1,16 @@
 // da_mma.cuh -- tensor-core consumer for packed GQA groups of G >= 4 query heads over bf16
 // caches, in both softmax modes.
 //
-// Per KV tile the group's work is two dense contractions ([G x d] . [d x T] for the logits,
-// [G x T] . [T x d] for P . V). On CUDA cores they made the split kernel ALU-bound on GB300
-// (the consumers alone, with no HBM traffic, took as long as the whole kernel), so for these
-// groups they run on the tensor cores with warp-level m16n8k16 bf16 MMAs:
-//   S^T-free form S = Q K^T: A = the group's q (rows = heads, padded to 16, unscaled bf16 so
-//   the operand is exact; the scale is applied to the FP32 logits), B = K rows read from the
-//   128-byte-swizzled TMA tile with ldmatrix;
-//   O += P V: A = P taken straight from the S accumulators (rows = heads, k = tokens), B = V
-//   rows read transposed with ldmatrix.trans.
+// Per KV tile the group's work is two dense contractions (the logits of G heads against the
+// tile's tokens, and P . V). On CUDA cores they made the split kernel issue-bound on GB300
+// (the consumers alone, with no HBM traffic, took about as long as the whole kernel), so for
+// these groups they run on the tensor cores with warp-level m16n8k16 bf16 MMAs, in transposed
+// form so that the 16 rows of the MMA are never wasted on a small group:
+//   S^T = K q^T: A = the warp's 16 K rows (8 of each of two stages) read with ldmatrix from
+//   the 128-byte-swizzled TMA tile, B = q^T (k = d, n = heads; unscaled bf16 so the operand is
+//   exact, the scale applied to the FP32 logits), 8 MMAs for d = 128;
+//   O^T += V^T P^T: A = V^T read with ldmatrix.trans (rows = d), B = P^T, which movmatrix
+//   transposes out of the S^T accumulator layout in registers; 8 m-tiles for d = 128.
 // O accumulates in the MMA registers across the whole piece. With one constant phi
 // (FlashDecoding++ Eq. 3 / Eq. 4) the accumulators are never rescaled. In the synchronised
 // mode each warp keeps a running maximum per head (the online-softmax recurrence of
@@ -17,8 +18,6 @@
 // accumulators and denominators by 2^(m_old - m_new), which after the first tiles is rare.
 // P enters the MMA as a bf16 pair p_hi + p_lo (p_lo = bf16 of the rounding residual), which
 // keeps P exact to ~2^-17; the softmax denominators are summed from the FP32 p.
-//
-// Each consumer warp takes 8 rows of two consecutive stages (16 tokens = one MMA k-extent).
 #pragma once
 
 #include "da_device.cuh"
@@ -39,15 +38,21 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "r"(addr));
 }
 
-// D += A (16x16, rows 8..15 zero) * B (16x8), bf16 inputs, FP32 accumulators.
-__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0,
-                                         uint32_t b1) {
-  const uint32_t z = 0u;
+// D += A (16x16) * B (16x8), bf16 inputs, FP32 accumulators.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
       "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(z), "r"(a2), "r"(z), "r"(b0), "r"(b1));
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Transpose of an 8x8 matrix of 16-bit values held in the warp's fragment layout.
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
 }
 
 // Two FP32 values -> bf16x2 (round to nearest even); `hi_elem` lands in the upper half.
@@ -57,27 +62,46 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo_elem, float hi_elem) {
   return r;
 }
 
-// Shared-memory address of element e (a multiple of 8) of row t in a tile written by a TMA box
-// of 64-element (128-byte) rows with the 128-byte swizzle: 128-byte row r = t * (D / 64) +
-// e / 64 stores its 16-byte chunk c at chunk c ^ (r mod 8). The tile base is 1024-aligned.
+// Byte offset of element e (a multiple of 8) of row t in a tile written by a TMA box of
+// 64-element (128-byte) rows with the 128-byte swizzle: 128-byte row r = t * (D / 64) + e / 64
+// stores its 16-byte chunk c at chunk c ^ (r mod 8). Tile bases are 1024-aligned.
 template <int D>
-__device__ __forceinline__ uint32_t swz(uint32_t base, int t, int e) {
+__device__ __forceinline__ uint32_t swz_off(int t, int e) {
   const int r = t * (D / 64) + e / 64;
   const int c = (e >> 3) & 7;
-  return base + (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+  return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
+
+// Per-lane constants of the warp's ldmatrix reads: lane l addresses row l % 8 of matrix l / 8.
+template <int D>
+struct MmaLane {
+  static constexpr int KS = D / 16;
+  uint32_t koff[KS];   // K tile, k-step kk: matrices (stage 0, d+0), (stage 1, d+0), (0, +8), (1, +8)
+  uint32_t voff[KS];   // V tile, m-tile mt: matrices (stage 0, d+0), (stage 0, +8), (1, +0), (1, +8)
+  int kst, vst;        // stage whose tile this lane's K / V row address lies in
+  __device__ __forceinline__ MmaLane(int row0, int lane) {
+    const int lmat = lane >> 3, t = row0 + (lane & 7);
+#pragma unroll
+    for (int i = 0; i < KS; ++i) {
+      koff[i] = swz_off<D>(t, i * 16 + (lmat >> 1) * 8);
+      voff[i] = swz_off<D>(t, i * 16 + (lmat & 1) * 8);
+    }
+    kst = lmat & 1;
+    vst = lmat >> 1;
+  }
+};
 
 template <int D, int G>
 struct MmaState {
-  static constexpr int KS = D / 16;     // MMA k-steps of the logits
-  static constexpr int NT = D / 8;      // 8-wide n-tiles of the output
-  uint32_t qa[KS][2];                   // A fragments of q (a0, a2); rows 8..15 are zero
-  float o[NT][4];                       // O accumulators (rows = heads; rows >= G unused)
-  float den;                            // this lane's share of its head's denominator
-  float m;                              // synchronised mode: its head's running maximum
+  static constexpr int KS = D / 16;     // k-steps of the logits / m-tiles of the output
+  uint32_t qb[KS][2];                   // B fragments of q^T (k = d, n = head); heads >= G zero
+  float o[KS][4];                       // O^T: [0] (d, head hp), [1] (d, hp + 1), [2] (d + 8, hp),
+                                        // [3] (d + 8, hp + 1) with d = 16 mt + lane / 4
+  float den[2];                         // this lane's share of heads hp, hp + 1 denominators
+  float m[2];                           // synchronised mode: their running maxima
 };
 
-// Load the group's q fragments from the stage's q area (G x D bf16, row-major, unscaled).
+// Load the group's q^T fragments from the stage's q area (G x D bf16, row-major, unscaled).
 template <int D, int G>
 __device__ __forceinline__ void mma_load_q(MmaState<D, G>& st, const uint8_t* qsm, int lane) {
   const int head = lane >> 2, kq = 2 * (lane & 3);
@@ -85,114 +109,111 @@ __device__ __forceinline__ void mma_load_q(MmaState<D, G>& st, const uint8_t* qs
 #pragma unroll
   for (int k = 0; k < MmaState<D, G>::KS; ++k) {
     const __nv_bfloat16* qr = reinterpret_cast<const __nv_bfloat16*>(qsm) + head * D + k * 16 + kq;
-    st.qa[k][0] = hv ? *reinterpret_cast<const uint32_t*>(qr) : 0u;
-    st.qa[k][1] = hv ? *reinterpret_cast<const uint32_t*>(qr + 8) : 0u;
+    st.qb[k][0] = hv ? *reinterpret_cast<const uint32_t*>(qr) : 0u;
+    st.qb[k][1] = hv ? *reinterpret_cast<const uint32_t*>(qr + 8) : 0u;
   }
 }
 
-// Consume the warp's 8 rows of two consecutive stages (n[1] == 0: no second stage; its rows are
-// masked and read stage 0's tile instead, so no stale shared memory enters the MMA).
+// Consume the warp's 8 rows of two consecutive stages (16 tokens = one MMA k-extent of P . V).
+// kt / vt: shared-memory addresses of the K and V tiles of stages 0 and 1 (with n[1] == 0 there
+// is no second stage: the caller passes stage 0's tiles again and every stage-1 token is
+// masked, so no stale shared memory enters the MMA).
 template <int D, int G, bool UNIFIED>
 __device__ __forceinline__ void mma_consume(const Params& p, MmaState<D, G>& st,
-                                            const uint8_t* const (&ks)[2],
-                                            const uint8_t* const (&vs)[2], const int (&n)[2],
-                                            int row0, int lane, uint32_t& fmask) {
+                                            const MmaLane<D>& ml, const uint32_t (&kt)[2],
+                                            const uint32_t (&vt)[2], const int (&n)[2], int row0,
+                                            int lane, uint32_t& fmask) {
   constexpr int KS = MmaState<D, G>::KS;
-  const uint32_t kb[2] = {smem_u32(ks[0]), smem_u32(n[1] > 0 ? ks[1] : ks[0])};
-  const uint32_t vb[2] = {smem_u32(vs[0]), smem_u32(n[1] > 0 ? vs[1] : vs[0])};
+  const uint32_t kbase = ml.kst ? kt[1] : kt[0], vbase = ml.vst ? vt[1] : vt[0];
 
-  // logits S = Q K^T for the 8 rows of each stage (one 16x8 accumulator per stage)
-  float s[2][4];
+  // S^T = K q^T: two accumulator chains (even and odd k-steps) halve the dependent latency
+  float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int b = 0; b < 2; ++b)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) s[b][i] = 0.f;
-  const int lrow = lane & 7, lmat = lane >> 3;
-#pragma unroll
-  for (int k2 = 0; k2 < KS / 2; ++k2) {
-#pragma unroll
-    for (int b = 0; b < 2; ++b) {
-      uint32_t r0, r1, r2, r3;
-      ldsm_x4(swz<D>(kb[b], row0 + lrow, k2 * 32 + lmat * 8), r0, r1, r2, r3);
-      mma_bf16(s[b], st.qa[2 * k2][0], st.qa[2 * k2][1], r0, r1);
-      mma_bf16(s[b], st.qa[2 * k2 + 1][0], st.qa[2 * k2 + 1][1], r2, r3);
-    }
+  for (int kk = 0; kk < KS; ++kk) {
+    uint32_t a0, a1, a2, a3;
+    ldsm_x4(kbase + ml.koff[kk], a0, a1, a2, a3);
+    if (kk & 1)
+      mma_bf16(sb, a0, a1, a2, a3, st.qb[kk][0], st.qb[kk][1]);
+    else
+      mma_bf16(sa, a0, a1, a2, a3, st.qb[kk][0], st.qb[kk][1]);
   }
 
-  // softmax on the accumulator elements this lane holds: head lane/4, tokens
-  // 2 (lane % 4) + {0, 1} of each stage; the quad of lanes 4h..4h+3 holds head h's 16 logits
-  const int head = lane >> 2, tk = 2 * (lane & 3);
-  const bool hv = head < G;
-  float x[2][2];
-  bool valid[2][2];
+  // The lane's logits: [0], [1] = token lane/4 of stage 0 for heads hp, hp + 1; [2], [3] = the
+  // same row of stage 1. A head's 16 logits sit in the 8 lanes that share lane % 4.
+  const int hp = 2 * (lane & 3), tr = row0 + (lane >> 2);
+  float x[4];
+  bool valid[4];
 #pragma unroll
-  for (int b = 0; b < 2; ++b)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      x[b][e] = s[b][e] * p.qscale;
-      valid[b][e] = hv && row0 + tk + e < n[b];
-    }
-  float ref = p.phi2;
+  for (int c = 0; c < 4; ++c) {
+    x[c] = (sa[c] + sb[c]) * p.qscale;
+    valid[c] = hp + (c & 1) < G && tr < n[c >> 1];
+  }
+  float ref0 = p.phi2, ref1 = p.phi2;
   if constexpr (!UNIFIED) {
-    float mx = -INFINITY;
+    float m0 = fmaxf(valid[0] ? x[0] : -INFINITY, valid[2] ? x[2] : -INFINITY);
+    float m1 = fmaxf(valid[1] ? x[1] : -INFINITY, valid[3] ? x[3] : -INFINITY);
 #pragma unroll
-    for (int b = 0; b < 2; ++b)
+    for (int o = 4; o <= 16; o <<= 1) {
+      m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+    }
+    const float n0 = fmaxf(st.m[0], m0), n1 = fmaxf(st.m[1], m1);
+    if (__any_sync(0xffffffffu, n0 > st.m[0] || n1 > st.m[1])) {
+      const float al0 = n0 > st.m[0] ? fast_exp2(st.m[0] - n0) : 1.f;   // 0 from -inf
+      const float al1 = n1 > st.m[1] ? fast_exp2(st.m[1] - n1) : 1.f;
 #pragma unroll
-      for (int e = 0; e < 2; ++e)
-        if (valid[b][e]) mx = fmaxf(mx, x[b][e]);
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const float m_new = fmaxf(st.m, mx);
-    if (__any_sync(0xffffffffu, m_new > st.m)) {
-      const float alpha = m_new > st.m ? fast_exp2(st.m - m_new) : 1.f;   // 0 from -inf
-#pragma unroll
-      for (int j = 0; j < MmaState<D, G>::NT; ++j) {
-        st.o[j][0] *= alpha;   // rows 8..15 ([2], [3]) stay zero
-        st.o[j][1] *= alpha;
+      for (int mt = 0; mt < KS; ++mt) {
+        st.o[mt][0] *= al0;
+        st.o[mt][1] *= al1;
+        st.o[mt][2] *= al0;
+        st.o[mt][3] *= al1;
       }
-      st.den *= alpha;
-      st.m = m_new;
+      st.den[0] *= al0;
+      st.den[1] *= al1;
+      st.m[0] = n0;
+      st.m[1] = n1;
     }
-    ref = st.m;   // -inf only while all of the head's tokens so far are masked
+    ref0 = st.m[0];   // -inf only while all of the head's tokens so far are masked
+    ref1 = st.m[1];
   }
-  float pr[2][2];
+  float pr[4];
 #pragma unroll
-  for (int b = 0; b < 2; ++b)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      pr[b][e] = valid[b][e] ? fast_exp2(x[b][e] - ref) : 0.f;
-      if (UNIFIED && valid[b][e] && (x[b][e] < p.lo2 || x[b][e] > p.hi2)) fmask |= 1u << head;
-      st.den += pr[b][e];
-    }
-  // P as A fragments (k = token: stage 0 rows in k 0..7, stage 1 rows in k 8..15), hi + lo
-  uint32_t ahi[2], alo[2];
-#pragma unroll
-  for (int b = 0; b < 2; ++b) {
-    ahi[b] = bf16x2_rn(pr[b][0], pr[b][1]);
-    const float h0 = __uint_as_float(ahi[b] << 16), h1 = __uint_as_float(ahi[b] & 0xffff0000u);
-    alo[b] = bf16x2_rn(pr[b][0] - h0, pr[b][1] - h1);
+  for (int c = 0; c < 4; ++c) {
+    pr[c] = valid[c] ? fast_exp2(x[c] - ((c & 1) ? ref1 : ref0)) : 0.f;
+    if (UNIFIED && valid[c] && (x[c] < p.lo2 || x[c] > p.hi2)) fmask |= 1u << (hp + (c & 1));
   }
-  // V rows of masked tokens are zeroed in the fragments (0 * NaN would poison the MMA)
-  uint32_t vm[2];
-#pragma unroll
-  for (int b = 0; b < 2; ++b)
-    vm[b] = (row0 + tk < n[b] ? 0x0000ffffu : 0u) | (row0 + tk + 1 < n[b] ? 0xffff0000u : 0u);
+  st.den[0] += pr[0] + pr[2];
+  st.den[1] += pr[1] + pr[3];
 
-  // O += P V, 16 output columns per ldmatrix.x4.trans: matrices (stage 0, cols +0..7),
-  // (stage 1, +0..7), (stage 0, +8..15), (stage 1, +8..15)
-  const int vst = lmat & 1, vcol = (lmat >> 1) * 8;
+  // P as bf16 hi + lo (lower half = head hp), transposed into B fragments of P^T:
+  // b0 = stage-0 tokens 2 (lane % 4), +1 of head lane / 4, b1 = the same of stage 1
+  const uint32_t h0 = bf16x2_rn(pr[0], pr[1]), h1 = bf16x2_rn(pr[2], pr[3]);
+  const uint32_t l0 = bf16x2_rn(pr[0] - __uint_as_float(h0 << 16),
+                                pr[1] - __uint_as_float(h0 & 0xffff0000u));
+  const uint32_t l1 = bf16x2_rn(pr[2] - __uint_as_float(h1 << 16),
+                                pr[3] - __uint_as_float(h1 & 0xffff0000u));
+  const uint32_t bh0 = movm_t(h0), bh1 = movm_t(h1), bl0 = movm_t(l0), bl1 = movm_t(l1);
+
+  // V rows of masked tokens are zeroed in the fragments (0 * NaN would poison the MMA); only
+  // a warp whose rows run past a stage's end needs it
+  uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+  if (!(row0 + kTokensPerWarp <= n[0] && row0 + kTokensPerWarp <= n[1])) {
+    const int tk = row0 + 2 * (lane & 3);
+    vm0 = (tk < n[0] ? 0x0000ffffu : 0u) | (tk + 1 < n[0] ? 0xffff0000u : 0u);
+    vm1 = (tk < n[1] ? 0x0000ffffu : 0u) | (tk + 1 < n[1] ? 0xffff0000u : 0u);
+  }
+
+  // O^T += V^T P^T: per m-tile of 16 d, A fragments (d 0-7 | 8-15) x (stage-0 | stage-1 tokens)
 #pragma unroll
-  for (int j2 = 0; j2 < D / 16; ++j2) {
-    uint32_t v0, v1, v2, v3;
-    ldsm_x4_t(swz<D>(vb[vst], row0 + lrow, j2 * 16 + vcol), v0, v1, v2, v3);
-    v0 &= vm[0];
-    v1 &= vm[1];
-    v2 &= vm[0];
-    v3 &= vm[1];
-    mma_bf16(st.o[2 * j2], ahi[0], ahi[1], v0, v1);
-    mma_bf16(st.o[2 * j2], alo[0], alo[1], v0, v1);
-    mma_bf16(st.o[2 * j2 + 1], ahi[0], ahi[1], v2, v3);
-    mma_bf16(st.o[2 * j2 + 1], alo[0], alo[1], v2, v3);
+  for (int mt = 0; mt < KS; ++mt) {
+    uint32_t a0, a1, a2, a3;
+    ldsm_x4_t(vbase + ml.voff[mt], a0, a1, a2, a3);
+    a0 &= vm0;
+    a1 &= vm0;
+    a2 &= vm1;
+    a3 &= vm1;
+    mma_bf16(st.o[mt], a0, a1, a2, a3, bh0, bh1);
+    mma_bf16(st.o[mt], a0, a1, a2, a3, bl0, bl1);
   }
 }
 
