@@ -244,6 +244,18 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// Atomic add with acquire-release semantics at GPU scope. After a CTA barrier, one thread's
+// call releases every write the CTA made before the barrier and acquires every write that
+// other CTAs released before their own calls on the same counter.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t* addr, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(addr), "r"(v)
+               : "memory");
+  return old;
+}
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ void pdl_launch_dependents() {

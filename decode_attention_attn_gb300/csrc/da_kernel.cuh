@@ -622,35 +622,50 @@ __device__ __forceinline__ void combine_piece(const Params& p, const Piece& pc, 
 
   if (!direct) {
     if (ctid == 0) __stcg(p.part_flags + pc.slot, fl);
-    __threadfence();
+    // Arrival: the barrier orders the CTA's partial writes before thread 0's release-acquire
+    // count; the last piece's count also acquires the other pieces' partials.
     named_bar_sync(1, kCT);
     if (ctid == 0) {
-      const int old = atomicAdd(p.counters + pc.g, 1);
+      const int old = atom_add_acq_rel_gpu(p.counters + pc.g, 1);
       misc[0] = old == pc.nslots - 1;
       misc[1] = 0;
     }
     named_bar_sync(1, kCT);
     if (misc[0]) {
-      // Last piece of the group: merge all its partials. Each pass issues all of its loads
-      // before using any, so the merge pays the L2 latency a few times, not per piece.
-      __threadfence();
+      // Last piece of the group: merge all its partials. Each thread owns EPT consecutive
+      // elements and issues the loads of up to 64 partial values at once, together with the
+      // LSEs, so a group of up to 64 / EPT pieces pays the L2 latency once.
       const int S = pc.nslots;
       float* wts = wbuf;              // [S, G] weights (scratch reused; S <= 8 * D)
       float* hsum = mm;               // [G] sum of weights
       float* hmax = ml;               // [G] maximum partial LSE
-      // O = sum_s w_s O_s / sum_s w_s: each thread owns EPT elements and keeps 32 partial
-      // loads in flight per block of pieces; the first block is loaded with the LSEs
-      constexpr int EPT = (G * D + kCT - 1) / kCT;
-      constexpr int SB = 32 / EPT;
-      const float* po = p.part_o + (long long)pc.slot_base * G * D;
-      float o[EPT][SB];
+      constexpr int EPT = G * D >= 4 * kCT ? 4 : (G * D >= 2 * kCT ? 2 : 1);
+      constexpr int SB = 64 / EPT;
+      const int e0 = ctid * EPT;
+      const bool owner = e0 < G * D;
+      const float* po = p.part_o + (long long)pc.slot_base * G * D + (owner ? e0 : 0);
+      float o[SB][EPT];
+      auto load_block = [&](int s0) {
 #pragma unroll
-      for (int i = 0; i < EPT; ++i) {
-        const int e = ctid + i * kCT;
-#pragma unroll
-        for (int j = 0; j < SB; ++j)
-          o[i][j] = (e < G * D && j < S) ? __ldcg(po + (long long)j * G * D + e) : 0.f;
-      }
+        for (int j = 0; j < SB; ++j) {
+          const bool ok = owner && s0 + j < S;
+          const float* src = po + (long long)(s0 + j) * G * D;
+          if constexpr (EPT == 4) {
+            const float4 v = ok ? __ldcg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            o[j][0] = v.x;
+            o[j][1] = v.y;
+            o[j][2] = v.z;
+            o[j][3] = v.w;
+          } else if constexpr (EPT == 2) {
+            const float2 v = ok ? __ldcg(reinterpret_cast<const float2*>(src)) : make_float2(0.f, 0.f);
+            o[j][0] = v.x;
+            o[j][1] = v.y;
+          } else {
+            o[j][0] = ok ? __ldcg(src) : 0.f;
+          }
+        }
+      };
+      load_block(0);
       const float* pl = p.part_l + (long long)pc.slot_base * G;
       for (int i = ctid; i < S * G; i += kCT) wts[i] = __ldcg(pl + i);
       uint32_t rf = 0;
@@ -679,41 +694,32 @@ __device__ __forceinline__ void combine_piece(const Params& p, const Piece& pc, 
         }
       }
       named_bar_sync(1, kCT);
+      const int g = owner ? e0 / D : 0;   // the thread's EPT elements share one head
       float num[EPT];
 #pragma unroll
       for (int i = 0; i < EPT; ++i) num[i] = 0.f;
       for (int s0 = 0; s0 < S; s0 += SB) {
-        if (s0 > 0) {
+        if (s0 > 0) load_block(s0);
 #pragma unroll
-          for (int i = 0; i < EPT; ++i) {
-            const int e = ctid + i * kCT;
+        for (int j = 0; j < SB; ++j) {
+          if (s0 + j < S) {
+            const float w = wts[(s0 + j) * G + g];
 #pragma unroll
-            for (int j = 0; j < SB; ++j)
-              o[i][j] = (e < G * D && s0 + j < S)
-                            ? __ldcg(po + (long long)(s0 + j) * G * D + e) : 0.f;
+            for (int i = 0; i < EPT; ++i) num[i] += w * o[j][i];
           }
-        }
-#pragma unroll
-        for (int i = 0; i < EPT; ++i) {
-          const int g = min(ctid + i * kCT, G * D - 1) / D;
-#pragma unroll
-          for (int j = 0; j < SB; ++j)
-            if (s0 + j < S) num[i] += wts[(s0 + j) * G + g] * o[i][j];
         }
       }
       const uint32_t rfa = (uint32_t)misc[1];
+      if (owner) {
+        const float sum = hsum[g];
+        const int d0 = e0 - g * D;
 #pragma unroll
-      for (int i = 0; i < EPT; ++i) {
-        const int e = ctid + i * kCT;
-        if (e < G * D) {
-          const int g = e / D, d = e - (e / D) * D;
-          const float sum = hsum[g];
-          store_out(p.out, (row0 + g) * D + d, p.out_dtype, sum > 0.f ? num[i] / sum : 0.f);
-          if (d == 0) {
-            if (p.out_lse)
-              p.out_lse[row0 + g] = sum > 0.f ? (hmax[g] + fast_log2(sum)) * kLn2 : -INFINITY;
-            if (p.row_flags && first_phase) p.row_flags[row0 + g] = (uint8_t)((rfa >> g) & 1u);
-          }
+        for (int i = 0; i < EPT; ++i)
+          store_out(p.out, (row0 + g) * D + d0 + i, p.out_dtype, sum > 0.f ? num[i] / sum : 0.f);
+        if (d0 == 0) {
+          if (p.out_lse)
+            p.out_lse[row0 + g] = sum > 0.f ? (hmax[g] + fast_log2(sum)) * kLn2 : -INFINITY;
+          if (p.row_flags && first_phase) p.row_flags[row0 + g] = (uint8_t)((rfa >> g) & 1u);
         }
       }
       if (ctid == 0) {
