@@ -160,6 +160,22 @@ def test_step_with_fewer_units_than_ctas(group, paged):
                    where=f"sparse G{group} paged={paged}")
 
 
+@pytest.mark.parametrize("group,head_dim", [(1, 128), (4, 64), (8, 64), (8, 128)])
+def test_merge_of_many_pieces(group, head_dim):
+    """100 uniform splits per group: the in-kernel merge takes its partials in several blocks
+    (more pieces than one block holds for every elements-per-thread width), and the last
+    splits of each sequence are empty."""
+    wl = workloads.Workload(f"many_G{group}_d{head_dim}", 1, 2 * group, 2, head_dim, "bf16",
+                            "bf16", seq_len=8192, num_splits=100)
+    inp = workloads.generate(wl, offset=5 * group + head_dim)
+    dev = _parity.DeviceInputs(inp)
+    ref, ref_lse, _, _ = _parity.run_oracle(inp)
+    for mode in ("sync", "unified"):
+        for od in ("bf16", "f32"):
+            _check(dev, ref, ref_lse, mode, out_dtype=od, num_splits=100, plan_splits=100,
+                   where=f"many pieces G{group} d{head_dim}")
+
+
 @pytest.mark.parametrize("page_size", [8, 16, 32, 64, 128])
 def test_page_sizes(page_size):
     wl = workloads.PAGED_B64.replace(name=f"pages{page_size}", batch=6, page_size=page_size,
