@@ -7,15 +7,18 @@
 // once, so each KV row is read from HBM once for the whole group ("FlashAttention and
 // inference kernels", Exercise 3).
 //
-// Warp roles:
-//   warp 8      producer: TMA-loads 64-row K and V tiles (and, per piece, the group's q)
-//               into a ring of shared-memory stages; paged caches are gathered through the
-//               block table one page per TMA box ("PagedAttention").
-//   warps 0..7  consumers: each takes 8 rows of every stage. A row of d elements is split
-//               over a lane group (16 lanes for d = 128 in 16-bit types, 16-byte chunks per
-//               lane); q . k partial sums for all heads and rows of the lane group are
-//               completed by a butterfly transpose-reduce that leaves one (row, head) logit
-//               per lane, so every lane does one exponential. Softmax:
+// Warp roles (12 warps; `setmaxnreg` moves registers from the producer warpgroup to the
+// consumers):
+//   warps 8..11 producers: two (contiguous cache) or four (paged cache) of them TMA-load
+//               64-row K and V tiles (and, per piece, the group's q) into a ring of
+//               shared-memory stages; paged caches are gathered through the block table one
+//               page per TMA box ("PagedAttention").
+//   warps 0..7  consumers: each takes 8 rows of every stage. For bf16 groups of 4 or 8 heads
+//               the logits and P . V run on the tensor cores (da_mma.cuh). Otherwise a row of
+//               d elements is split over a lane group (16 lanes for d = 128 in 16-bit types,
+//               16-byte chunks per lane); q . k partial sums for all heads and rows of the
+//               lane group are completed by a transpose-reduce through shared memory that
+//               leaves whole (row, head) logits per lane. Softmax:
 //                 SYNC    -- online softmax with the running maximum per head, rescaling
 //                            the accumulators by exp(m_old - m_new) ("FlashAttention:
 //                            tiling plus online softmax");
@@ -56,34 +59,6 @@ struct Cfg {
   static_assert((kTokensPerWarp % kNlg) == 0, "rows per warp must split over lane groups");
   static_assert((kV & (kV - 1)) == 0, "logit count must be a power of two");
   static_assert((kQBytes % 16) == 0, "q bulk copy must be a multiple of 16 bytes");
-};
-
-// Butterfly transpose-reduce over the O*2 lanes of a lane group. Each lane starts with N
-// partial sums (index = row * G + head); at every step a lane keeps half of its values
-// (the upper half if its lane bit O is set), sends the other half to its partner and adds
-// what it receives. After log2(N) halvings each lane holds complete sums of consecutive
-// indices; further steps are plain butterfly adds (lanes then hold replicated values).
-template <int N, int O>
-struct Reduce {
-  __device__ __forceinline__ static void run(float* v, int lane) {
-    if constexpr (O == 0) {
-      return;
-    } else if constexpr (N > 1) {
-      constexpr int H = N / 2;
-      const bool upper = (lane & O) != 0;
-#pragma unroll
-      for (int i = 0; i < H; ++i) {
-        const float a = v[i], b = v[i + H];
-        const float send = upper ? a : b;
-        const float keep = upper ? b : a;
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
-      }
-      Reduce<H, O / 2>::run(v, lane);
-    } else {
-      v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
-      Reduce<1, O / 2>::run(v, lane);
-    }
-  }
 };
 
 struct Piece {
