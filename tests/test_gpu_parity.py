@@ -233,6 +233,37 @@ def test_forced_fallback_every_row():
     assert st2.rows_flagged == 0 and not flags2.cpu().numpy().any()
 
 
+def test_some_rows_flagged_in_a_paged_batch():
+    """A few K rows point along one query head's direction, so exactly those rows (a head in
+    each of two groups of different sequences, two heads of one of them) leave [lo, hi]: the
+    list holds only their groups, the recompute covers them, the other groups keep their
+    unified results, and the flags are exact per row."""
+    wl = workloads.Workload("someflags", 6, 32, 8, 128, "bf16", "bf16", lens=(900, 3000, 17, 2500, 640, 1),
+                            paged=True, page_size=16, mode="unified")
+    inp = workloads.generate(wl, offset=21)
+    G, P = 4, 16
+    # (sequence, kv head, token, head within the group)
+    plant = [(1, 2, 100, 1), (3, 5, 2000, 3), (3, 5, 7, 0)]
+    for b, kvh, t, hg in plant:
+        qh = inp.q[b, kvh * G + hg].float()
+        row = inp.block_table[b, t // P].item()
+        inp.k_cache[row, t % P, kvh] = (12.0 * qh / qh.norm()).to(torch.bfloat16)
+    phi, lo, hi = 0.0, -30.0, 8.0
+    dev = _parity.DeviceInputs(inp)
+    ref, ref_lse, ref_flag, margin = _parity.run_oracle(inp, phi=phi, lo=lo, hi=hi)
+    flagged = {(b, kvh * G + hg) for b, kvh, _, hg in plant}
+    got_rows = {(int(i) // 32, int(i) % 32) for i in np.flatnonzero(ref_flag)}
+    assert flagged <= got_rows and len(got_rows) <= 8   # the planted rows, a few neighbours at most
+    assert _parity.margin_ok(margin).all()
+    for od in ("bf16", "f32"):
+        out, lse, flags, st = _parity.run_gpu(dev, out_dtype=od, want_stats=True,
+                                              phi=phi, lo=lo, hi=hi)
+        _parity.compare(out, ref.reshape(out.shape), od, where=f"some rows flagged {od}")
+        _parity.compare_lse(lse, ref_lse.reshape(lse.shape), where="some rows flagged")
+        assert np.array_equal(flags.cpu().numpy().ravel().astype(bool), ref_flag.astype(bool))
+        assert st.rows_flagged == int(ref_flag.sum())
+
+
 def test_underflow_injection_is_flagged_and_finite():
     # every logit far below phi + lo: the unified exponentials would underflow to zero
     wl = workloads.Workload("underflow", 1, 4, 1, 128, "bf16", "bf16", seq_len=700,
