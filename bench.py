@@ -45,7 +45,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gqa32k")
-    ap.add_argument("--mode", default="unified", choices=["unified", "sync"])
+    ap.add_argument("--mode", default="unified", choices=["unified", "sync", "unified_local"])
     ap.add_argument("--num-splits", type=int, default=-1,
                     help="-1: the plan's heuristic; >0 uniform splits")
     ap.add_argument("--no-e2e", action="store_true")

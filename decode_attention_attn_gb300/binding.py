@@ -15,12 +15,13 @@ from typing import Optional
 from . import build as _build
 
 DA_F32, DA_F16, DA_BF16 = 0, 1, 2
-DA_SOFTMAX_SYNC, DA_SOFTMAX_UNIFIED = 0, 1
+DA_SOFTMAX_SYNC, DA_SOFTMAX_UNIFIED, DA_SOFTMAX_UNIFIED_LOCAL = 0, 1, 2
 ERRORS = {0: "DA_OK", -1: "DA_ERR_INVALID_ARG", -2: "DA_ERR_UNSUPPORTED",
           -3: "DA_ERR_WORKSPACE_TOO_SMALL", -4: "DA_ERR_BAD_BLOCK_TABLE", -5: "DA_ERR_CUDA",
           -6: "DA_ERR_DEVICE_TIMEOUT", -7: "DA_ERR_BAD_SEQ_LEN"}
 DTYPE_CODES = {"f32": DA_F32, "f16": DA_F16, "bf16": DA_BF16}
-MODE_CODES = {"sync": DA_SOFTMAX_SYNC, "unified": DA_SOFTMAX_UNIFIED}
+MODE_CODES = {"sync": DA_SOFTMAX_SYNC, "unified": DA_SOFTMAX_UNIFIED,
+              "unified_local": DA_SOFTMAX_UNIFIED_LOCAL}
 
 
 class DecodeAttnError(RuntimeError):

@@ -18,9 +18,9 @@
 #include "da_device.cuh"
 
 namespace da {
-const void* kernel_f32(int head_dim, int group, bool unified);
-const void* kernel_f16(int head_dim, int group, bool unified);
-const void* kernel_bf16(int head_dim, int group, bool unified);
+const void* kernel_f32(int head_dim, int group, int mode);
+const void* kernel_f16(int head_dim, int group, int mode);
+const void* kernel_bf16(int head_dim, int group, int mode);
 
 // The element offset the kernel reads token t of (b, kvh) from: the same token_row() the
 // producer warp uses for its TMA box coordinates.
@@ -95,7 +95,9 @@ int validate_problem(const da_problem& p) {
   if (p.head_dim != 64 && p.head_dim != 128) return DA_ERR_UNSUPPORTED;
   if (p.qkv_dtype < DA_F32 || p.qkv_dtype > DA_BF16) return DA_ERR_UNSUPPORTED;
   if (p.out_dtype < DA_F32 || p.out_dtype > DA_BF16) return DA_ERR_UNSUPPORTED;
-  if (p.mode != DA_SOFTMAX_SYNC && p.mode != DA_SOFTMAX_UNIFIED) return DA_ERR_INVALID_ARG;
+  if (p.mode != DA_SOFTMAX_SYNC && p.mode != DA_SOFTMAX_UNIFIED &&
+      p.mode != DA_SOFTMAX_UNIFIED_LOCAL)
+    return DA_ERR_INVALID_ARG;
   if (p.num_sms < 0) return DA_ERR_INVALID_ARG;
   if (p.paged) {
     if (!is_pow2(p.page_size) || p.page_size < 8 || p.page_size > 256) return DA_ERR_UNSUPPORTED;
@@ -106,7 +108,7 @@ int validate_problem(const da_problem& p) {
     if (p.max_seq_len < 1) return DA_ERR_INVALID_ARG;
     if ((long long)p.batch * p.max_seq_len >= (1ll << 31)) return DA_ERR_INVALID_ARG;
   }
-  if (p.mode == DA_SOFTMAX_UNIFIED) {
+  if (p.mode != DA_SOFTMAX_SYNC) {
     if (!std::isfinite(p.unified_max) || !std::isfinite(p.range_lo) ||
         !std::isfinite(p.range_hi) || !(p.range_lo < p.range_hi))
       return DA_ERR_INVALID_ARG;
@@ -114,11 +116,11 @@ int validate_problem(const da_problem& p) {
   return DA_OK;
 }
 
-const void* kernel_for(const da_plan& pl, bool unified) {
+const void* kernel_for(const da_plan& pl, int mode) {
   switch (pl.prob.qkv_dtype) {
-    case DA_F32: return kernel_f32(pl.prob.head_dim, pl.group, unified);
-    case DA_F16: return kernel_f16(pl.prob.head_dim, pl.group, unified);
-    case DA_BF16: return kernel_bf16(pl.prob.head_dim, pl.group, unified);
+    case DA_F32: return kernel_f32(pl.prob.head_dim, pl.group, mode);
+    case DA_F16: return kernel_f16(pl.prob.head_dim, pl.group, mode);
+    case DA_BF16: return kernel_bf16(pl.prob.head_dim, pl.group, mode);
   }
   return nullptr;
 }
@@ -466,7 +468,7 @@ int decode_attn_run_ex(const da_plan* plan, const da_run_args* args) {
     S = num_splits;
   }
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
-  const bool unified = p.mode == DA_SOFTMAX_UNIFIED;
+  const bool unified = p.mode == DA_SOFTMAX_UNIFIED;   // the recompute launch follows
 
   // tensor-core kernels (both modes, so the recompute pass too) read 128-byte-swizzled tiles
   const bool mma = uses_mma(pl.es, p.qkv_dtype == DA_BF16, pl.group);
@@ -483,6 +485,7 @@ int decode_attn_run_ex(const da_plan* plan, const da_run_args* args) {
   kp.row_flags = row_flags;
   kp.policy = policy;
   kp.num_splits = S;
+  kp.list_flags = unified ? 1 : 0;
   const double log2e = 1.4426950408889634;
   kp.qscale = (float)((double)scale * log2e);
   kp.phi2 = (float)((double)p.unified_max * log2e);
@@ -501,7 +504,7 @@ int decode_attn_run_ex(const da_plan* plan, const da_run_args* args) {
   }
 
   // The split kernel computes the step; the last piece of each group merges it in-kernel.
-  const void* fn = kernel_for(pl, unified);
+  const void* fn = kernel_for(pl, p.mode);
   if (!fn) return DA_ERR_UNSUPPORTED;
   rc = ensure_smem_attr(fn, pl.smem_bytes);
   if (rc != DA_OK) return rc;
@@ -530,7 +533,7 @@ int decode_attn_run_ex(const da_plan* plan, const da_run_args* args) {
     rp.policy = kUniform;
     rp.num_splits = pl.recompute_splits;
     rp.recompute = 1;
-    const void* rfn = kernel_for(pl, false);
+    const void* rfn = kernel_for(pl, DA_SOFTMAX_SYNC);
     rc = ensure_smem_attr(rfn, pl.smem_bytes);
     if (rc != DA_OK) return rc;
     cudaLaunchAttribute pdl[1];

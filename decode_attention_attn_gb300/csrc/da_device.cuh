@@ -41,6 +41,8 @@ constexpr int kStatusTimeout = 4;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 enum Policy { kBalanced = 0, kUniform = 1 };
+// Softmax modes, numbered as the C ABI's da_softmax_mode.
+enum SoftmaxMode { kSoftmaxSync = 0, kSoftmaxUnified = 1, kSoftmaxUnifiedLocal = 2 };
 enum OutType { kOutF32 = 0, kOutF16 = 1, kOutBF16 = 2 };
 
 struct Params {
@@ -70,6 +72,7 @@ struct Params {
   int policy;                    // kBalanced / kUniform
   int num_splits;                // uniform: splits per group
   int recompute;                 // 1: the recompute launch (groups from the flagged list)
+  int list_flags;                // 1: flagged groups go to the list (a recompute launch follows)
   int n_groups;                  // B * Hkv
   int stages;                    // pipeline depth
   int batch_smem;                // lengths held in smem (balanced) or 0

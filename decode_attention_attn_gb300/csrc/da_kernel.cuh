@@ -279,14 +279,15 @@ struct LaneMap {
 // of the second batch, which then reads stale but in-bounds shared memory). p values are
 // published to shared memory as (p, p) pairs so that P . V takes its packed-FMA operands
 // straight from a 16-byte load.
-template <typename T, int D, int G, bool UNIFIED>
+template <typename T, int D, int G, bool UNIFIED, bool LOCAL>
 __device__ __forceinline__ void consume_stages(const Params& p, const LaneMap<T, D, G>& lm,
                                                const uint8_t* const (&ks)[2],
                                                const uint8_t* const (&vs)[2], const int (&n)[2],
                                                const f32x2 (&q2)[G][Cfg<T, D, G>::kEpl / 2],
                                                f32x2 (&acc2)[G][Cfg<T, D, G>::kEpl / 2],
                                                float (&dl)[Cfg<T, D, G>::kNv], float (&m)[G],
-                                               uint32_t& fmask, float* wscr) {
+                                               float (&mt)[G], bool& sw, uint32_t& fmask,
+                                               float* wscr) {
   using C = Cfg<T, D, G>;
   constexpr int E2 = C::kEpl / 2;
   constexpr int RS = tp_row_stride(D, C::kEs);
@@ -348,7 +349,53 @@ __device__ __forceinline__ void consume_stages(const Params& p, const LaneMap<T,
 #pragma unroll
     for (int i = 0; i < C::kNv; ++i) valid[b][i] = lm.row0 + lm.j[i] < n[b];
 
-  if constexpr (UNIFIED) {
+  bool use_sync = !UNIFIED;
+  if constexpr (LOCAL) {
+    // Split-local fallback: while every logit so far was in range, the state is an exact
+    // online-softmax state with m = phi. On the first tile with a logit out of range the warp
+    // rescales it to each head's true maximum so far and continues with the synchronised
+    // recurrence, so the split needs no second read of its KV.
+    if (!sw) {
+      bool out = false;
+#pragma unroll
+      for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int i = 0; i < C::kNv; ++i)
+          if (valid[b][i]) {
+            const float sv = sc[b][i];
+            out = out || sv < p.lo2 || sv > p.hi2;
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+              if (lm.g[i] == g) mt[g] = fmaxf(mt[g], sv);
+          }
+      if (__any_sync(0xffffffffu, out)) {
+        float alpha[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float mg = mt[g];
+#pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) mg = fmaxf(mg, __shfl_xor_sync(0xffffffffu, mg, o));
+          alpha[g] = mg > -INFINITY ? fast_exp2(p.phi2 - mg) : 1.f;
+          m[g] = mg;
+          const f32x2 a2 = f2_pack(alpha[g], alpha[g]);
+#pragma unroll
+          for (int e = 0; e < E2; ++e) acc2[g][e] = f2_mul(acc2[g][e], a2);
+        }
+#pragma unroll
+        for (int i = 0; i < C::kNv; ++i) {
+          float ag = alpha[0];
+#pragma unroll
+          for (int g = 1; g < G; ++g)
+            if (lm.g[i] == g) ag = alpha[g];
+          dl[i] *= ag;
+        }
+        sw = true;
+      }
+    }
+    use_sync = sw;
+  }
+
+  if (!use_sync) {
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
       float2* pw = pwarp + b * kTokensPerWarp * G + lm.lg * C::kV;
@@ -368,6 +415,7 @@ __device__ __forceinline__ void consume_stages(const Params& p, const LaneMap<T,
 #pragma unroll
       for (int i = 0; i < C::kNv; ++i) {
         const float s = valid[b][i] ? sc[b][i] : -INFINITY;
+        if (UNIFIED && valid[b][i] && (s < p.lo2 || s > p.hi2)) fmask |= 1u << lm.g[i];
         if (lm.writer) pw[lm.idx(i)] = make_float2(s, s);
       }
     }
@@ -590,8 +638,10 @@ __device__ __forceinline__ void combine_piece(const Params& p, const Piece& pc, 
     atomicAdd(p.stats + 1, (unsigned long long)__popc(fl));
     if (direct) {
       atomicAdd(p.stats + 0, (unsigned long long)__popc(fl));
-      const int at = atomicAdd(p.list_state, 1);
-      if (at < p.n_groups) p.flag_list[at] = pc.g;
+      if (p.list_flags) {
+        const int at = atomicAdd(p.list_state, 1);
+        if (at < p.n_groups) p.flag_list[at] = pc.g;
+      }
     }
   }
 
@@ -701,8 +751,10 @@ __device__ __forceinline__ void combine_piece(const Params& p, const Piece& pc, 
         p.counters[pc.g] = 0;   // leave the counter ready for the next run
         if (first_phase && rfa) {
           atomicAdd(p.stats + 0, (unsigned long long)__popc(rfa));
-          const int at = atomicAdd(p.list_state, 1);
-          if (at < p.n_groups) p.flag_list[at] = pc.g;
+          if (p.list_flags) {
+            const int at = atomicAdd(p.list_state, 1);
+            if (at < p.n_groups) p.flag_list[at] = pc.g;
+          }
         }
       }
     }
@@ -710,7 +762,7 @@ __device__ __forceinline__ void combine_piece(const Params& p, const Piece& pc, 
   named_bar_sync(1, kCT);   // shared scratch is free for the next piece
 }
 
-template <typename T, int D, int G, bool UNIFIED>
+template <typename T, int D, int G, bool UNIFIED, bool LOCAL>
 __device__ __forceinline__ void run_consumers(const Params& p, Sched s, uint8_t* stages,
                                               const Layout& L, uint64_t* full, uint64_t* empty,
                                               uint8_t* smem, int warp, int lane, uint32_t& k,
@@ -729,11 +781,13 @@ __device__ __forceinline__ void run_consumers(const Params& p, Sched s, uint8_t*
   Piece pc;
   constexpr int E2 = E / 2;
   while (sched_next(s, p, pc)) {
-    float dl[C::kNv], m[G];
+    float dl[C::kNv], m[G], mt[G];
+    bool sw = false;
     f32x2 acc2[G][E2], q2[G][E2];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       m[g] = UNIFIED ? p.phi2 : -INFINITY;
+      mt[g] = -INFINITY;
 #pragma unroll
       for (int e = 0; e < E2; ++e) {
         acc2[g][e] = 0ull;   // +0.0f in both halves
@@ -774,7 +828,8 @@ __device__ __forceinline__ void run_consumers(const Params& p, Sched s, uint8_t*
       const uint8_t* const kss[2] = {st0 + L.k_off, st1 + L.k_off};
       const uint8_t* const vss[2] = {st0 + L.v_off, st1 + L.v_off};
       if (!dead)
-        consume_stages<T, D, G, UNIFIED>(p, lm, kss, vss, n, q2, acc2, dl, m, fmask, wscr);
+        consume_stages<T, D, G, UNIFIED, LOCAL>(p, lm, kss, vss, n, q2, acc2, dl, m, mt, sw,
+                                                fmask, wscr);
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&empty[s0]);
@@ -794,7 +849,7 @@ __device__ __forceinline__ void run_consumers(const Params& p, Sched s, uint8_t*
 
 // Tensor-core consumers (unified softmax, bf16, G >= 4): same stage-pair loop as
 // run_consumers, the math in mma_consume.
-template <typename T, int D, int G, bool UNIFIED>
+template <typename T, int D, int G, bool UNIFIED, bool LOCAL>
 __device__ __forceinline__ void run_consumers_mma(const Params& p, Sched s, uint8_t* stages,
                                                   const Layout& L, uint64_t* full,
                                                   uint64_t* empty, uint8_t* smem, int warp,
@@ -817,6 +872,8 @@ __device__ __forceinline__ void run_consumers_mma(const Params& p, Sched s, uint
       for (int i = 0; i < 4; ++i) st.o[j][i] = 0.f;
     st.den[0] = st.den[1] = 0.f;
     st.m[0] = st.m[1] = -INFINITY;
+    st.mt[0] = st.mt[1] = -INFINITY;
+    st.sw = false;
     uint32_t fmask = 0;
     const int nst = (pc.t1 - pc.t0 + kStageTokens - 1) / kStageTokens;
     for (int j = 0; j < nst; j += 2) {
@@ -839,7 +896,7 @@ __device__ __forceinline__ void run_consumers_mma(const Params& p, Sched s, uint
       const uint8_t* const st1m = pair ? st1 : st0;   // no second stage: read stage 0 again
       const uint32_t kt[2] = {smem_u32(st0 + L.k_off), smem_u32(st1m + L.k_off)};
       const uint32_t vt[2] = {smem_u32(st0 + L.v_off), smem_u32(st1m + L.v_off)};
-      if (!dead) mma_consume<D, G, UNIFIED>(p, st, mlane, kt, vt, n, row0, lane, fmask);
+      if (!dead) mma_consume<D, G, UNIFIED, LOCAL>(p, st, mlane, kt, vt, n, row0, lane, fmask);
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&empty[s0]);
@@ -847,8 +904,9 @@ __device__ __forceinline__ void run_consumers_mma(const Params& p, Sched s, uint
       }
       k += pair ? 2u : 1u;
     }
-    publish_mma<T, D, G>(st, UNIFIED ? p.phi2 : st.m[0], UNIFIED ? p.phi2 : st.m[1], fmask, mm,
-                         ml, mflag, wbuf, warp, lane);
+    const bool at_phi = UNIFIED && !(LOCAL && st.sw);   // the state is relative to phi
+    publish_mma<T, D, G>(st, at_phi ? p.phi2 : st.m[0], at_phi ? p.phi2 : st.m[1], fmask, mm, ml,
+                         mflag, wbuf, warp, lane);
     combine_piece<T, D, G>(p, pc, s.first_phase, mm, ml, mflag, wbuf, misc, warp, lane, ctid);
   }
 }
@@ -896,8 +954,9 @@ __device__ __forceinline__ Sched launch_sched(const Params& p, const int* lens, 
 }
 
 // A consumer warp's role over the launch's pieces.
-template <typename T, int D, int G, bool UNIFIED>
+template <typename T, int D, int G, int MODE>
 __device__ __forceinline__ void consumer_role(const Params& p, int warp, int lane) {
+  constexpr bool UNIFIED = MODE != kSoftmaxSync, LOCAL = MODE == kSoftmaxUnifiedLocal;
   using C = Cfg<T, D, G>;
   constexpr bool kMma = uses_mma(sizeof(T), std::is_same<T, __nv_bfloat16>::value, G);
   uint8_t* smem = smem_base();
@@ -910,9 +969,11 @@ __device__ __forceinline__ void consumer_role(const Params& p, int warp, int lan
   uint32_t k = 0;
   bool dead = false;
   if constexpr (kMma)
-    run_consumers_mma<T, D, G, UNIFIED>(p, s, smem, L, full, empty, smem, warp, lane, k, dead);
+    run_consumers_mma<T, D, G, UNIFIED, LOCAL>(p, s, smem, L, full, empty, smem, warp, lane, k,
+                                               dead);
   else
-    run_consumers<T, D, G, UNIFIED>(p, s, smem, L, full, empty, smem, warp, lane, k, dead);
+    run_consumers<T, D, G, UNIFIED, LOCAL>(p, s, smem, L, full, empty, smem, warp, lane, k,
+                                           dead);
 }
 
 // A producer-warpgroup warp's role (two warps issue copies for a contiguous cache, four for a
@@ -943,7 +1004,7 @@ __device__ __forceinline__ void producer_role(const Params& p, const CUtensorMap
 // list of groups whose range check failed and recomputes them with the synchronised softmax
 // as uniform splits ("The Overflow Fallback: Recomputation"); with nothing flagged it exits
 // at once.
-template <typename T, int D, int G, bool UNIFIED>
+template <typename T, int D, int G, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_split_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv) {
@@ -1024,7 +1085,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // 12 * 32 * 168 (checked on the host before the first launch).
   if (warp < kConsumerWarps) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
-    consumer_role<T, D, G, UNIFIED>(p, warp, lane);
+    consumer_role<T, D, G, MODE>(p, warp, lane);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
     producer_role<T, D, G>(p, &tmk, &tmv, warp, lane);
@@ -1044,11 +1105,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <typename T, int D>
-inline const void* pick_kernel(int G, bool unified) {
-#define DA_CASE(GG)                                                             \
-  case GG:                                                                      \
-    return unified ? (const void*)&decode_split_kernel<T, D, GG, true>          \
-                   : (const void*)&decode_split_kernel<T, D, GG, false>;
+inline const void* pick_kernel(int G, int mode) {
+#define DA_CASE(GG)                                                                      \
+  case GG:                                                                               \
+    return mode == kSoftmaxSync      ? (const void*)&decode_split_kernel<T, D, GG, 0>    \
+           : mode == kSoftmaxUnified ? (const void*)&decode_split_kernel<T, D, GG, 1>    \
+                                     : (const void*)&decode_split_kernel<T, D, GG, 2>;
   switch (G) {
     DA_CASE(1)
     DA_CASE(2)

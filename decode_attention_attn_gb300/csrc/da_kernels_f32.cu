@@ -3,9 +3,9 @@
 
 namespace da {
 
-const void* kernel_f32(int head_dim, int group, bool unified) {
-  if (head_dim == 64) return pick_kernel<float, 64>(group, unified);
-  if (head_dim == 128) return pick_kernel<float, 128>(group, unified);
+const void* kernel_f32(int head_dim, int group, int mode) {
+  if (head_dim == 64) return pick_kernel<float, 64>(group, mode);
+  if (head_dim == 128) return pick_kernel<float, 128>(group, mode);
   return nullptr;
 }
 

@@ -98,7 +98,11 @@ struct MmaState {
   float o[KS][4];                       // O^T: [0] (d, head hp), [1] (d, hp + 1), [2] (d + 8, hp),
                                         // [3] (d + 8, hp + 1) with d = 16 mt + lane / 4
   float den[2];                         // this lane's share of heads hp, hp + 1 denominators
-  float m[2];                           // synchronised mode: their running maxima
+  float m[2];                           // synchronised recurrence: their running maxima
+  float mt[2];                          // split-local fallback, before the switch: the lane's
+                                        // maximum logit of each head so far
+  bool sw;                              // split-local fallback: the warp has switched to the
+                                        // synchronised recurrence
 };
 
 // Load the group's q^T fragments from the stage's q area (G x D bf16, row-major, unscaled).
@@ -118,7 +122,7 @@ __device__ __forceinline__ void mma_load_q(MmaState<D, G>& st, const uint8_t* qs
 // kt / vt: shared-memory addresses of the K and V tiles of stages 0 and 1 (with n[1] == 0 there
 // is no second stage: the caller passes stage 0's tiles again and every stage-1 token is
 // masked, so no stale shared memory enters the MMA).
-template <int D, int G, bool UNIFIED>
+template <int D, int G, bool UNIFIED, bool LOCAL>
 __device__ __forceinline__ void mma_consume(const Params& p, MmaState<D, G>& st,
                                             const MmaLane<D>& ml, const uint32_t (&kt)[2],
                                             const uint32_t (&vt)[2], const int (&n)[2], int row0,
@@ -149,7 +153,45 @@ __device__ __forceinline__ void mma_consume(const Params& p, MmaState<D, G>& st,
     valid[c] = hp + (c & 1) < G && tr < n[c >> 1];
   }
   float ref0 = p.phi2, ref1 = p.phi2;
-  if constexpr (!UNIFIED) {
+  if constexpr (LOCAL) {
+    // Split-local fallback: while every logit so far was in range, the state is an exact
+    // online-softmax state with m = phi. On the first tile with a logit out of range the warp
+    // rescales it to the true maximum so far and continues with the synchronised recurrence,
+    // so the split needs no second read of its KV.
+    if (!st.sw) {
+      bool out = false;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (valid[c]) {
+          out = out || x[c] < p.lo2 || x[c] > p.hi2;
+          st.mt[c & 1] = fmaxf(st.mt[c & 1], x[c]);
+        }
+      }
+      if (__any_sync(0xffffffffu, out)) {
+        float m0 = st.mt[0], m1 = st.mt[1];
+#pragma unroll
+        for (int o = 4; o <= 16; o <<= 1) {
+          m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+          m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+        }
+        const float al0 = m0 > -INFINITY ? fast_exp2(p.phi2 - m0) : 1.f;
+        const float al1 = m1 > -INFINITY ? fast_exp2(p.phi2 - m1) : 1.f;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          st.o[mt][0] *= al0;
+          st.o[mt][1] *= al1;
+          st.o[mt][2] *= al0;
+          st.o[mt][3] *= al1;
+        }
+        st.den[0] *= al0;
+        st.den[1] *= al1;
+        st.m[0] = m0;
+        st.m[1] = m1;
+        st.sw = true;
+      }
+    }
+  }
+  if (!UNIFIED || (LOCAL && st.sw)) {
     float m0 = fmaxf(valid[0] ? x[0] : -INFINITY, valid[2] ? x[2] : -INFINITY);
     float m1 = fmaxf(valid[1] ? x[1] : -INFINITY, valid[3] ? x[3] : -INFINITY);
 #pragma unroll

@@ -43,7 +43,7 @@ class Workload:
     paged: bool = False
     page_size: int = 16
     num_splits: int = 0             # 0: the library's heuristic; >0: that many splits
-    mode: str = "sync"              # "sync" or "unified"
+    mode: str = "sync"              # "sync", "unified" or "unified_local"
     phi: float = -3.9               # unified max constant (natural-log units)
     range_lo: float = -64.0         # closed in-range interval on (x - phi)
     range_hi: float = 64.0

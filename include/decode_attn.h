@@ -54,8 +54,19 @@ typedef enum { DA_F32 = 0, DA_F16 = 1, DA_BF16 = 2 } da_dtype;
  *   unified_max, with no maximum and no rescaling (FlashDecoding++ Eq. 3 and Eq. 4). A
  *   scaled logit x with x - phi < range_lo or x - phi > range_hi (the interval is
  *   closed: a value on a bound is in range, as in Fig. 6) flags its row; flagged rows are
- *   recomputed in DA_SOFTMAX_SYNC mode on the device, in the same call. */
-typedef enum { DA_SOFTMAX_SYNC = 0, DA_SOFTMAX_UNIFIED = 1 } da_softmax_mode;
+ *   recomputed in DA_SOFTMAX_SYNC mode on the device, in the same call ("The Overflow
+ *   Fallback: Recomputation").
+ * DA_SOFTMAX_UNIFIED_LOCAL: as DA_SOFTMAX_UNIFIED, with the same row flags, but without the
+ *   second pass: a unified partial whose logits were all in range is an exact online-softmax
+ *   state with maximum phi, so on its first out-of-range logit each split rescales its state
+ *   to the true maximum so far and continues with the synchronised recurrence, reading no
+ *   KV twice. An extension of the FlashDecoding++ fallback (the outputs equal the plain
+ *   softmax either way). */
+typedef enum {
+  DA_SOFTMAX_SYNC = 0,
+  DA_SOFTMAX_UNIFIED = 1,
+  DA_SOFTMAX_UNIFIED_LOCAL = 2
+} da_softmax_mode;
 
 enum {
   DA_OK = 0,
@@ -85,7 +96,7 @@ typedef struct {
   da_dtype qkv_dtype;       /* storage of q, k_cache and v_cache */
   da_dtype out_dtype;       /* storage of out (rounded to nearest even from fp32) */
   da_softmax_mode mode;
-  float unified_max;        /* phi (natural-log units of the scaled logits); UNIFIED only */
+  float unified_max;        /* phi (natural-log units of the scaled logits); UNIFIED modes */
   float range_lo;           /* closed in-range interval on x - phi; range_lo < range_hi */
   float range_hi;
   int validate;             /* 1: every run synchronises and reports device findings */
@@ -115,7 +126,7 @@ typedef struct {
   int num_splits;           /* as in da_plan_info, for this run */
   long long rows_flagged;   /* UNIFIED: (b, h) rows whose range check failed */
   long long splits_flagged; /* UNIFIED: (split, h) partials whose range check failed */
-  int recompute_launched;   /* 1 iff the recompute kernel was enqueued (UNIFIED) */
+  int recompute_launched;   /* 1 iff the recompute kernel was enqueued (DA_SOFTMAX_UNIFIED) */
 } da_stats;
 
 /* Validate a problem and choose the launch (grid, split policy, pipeline) for it.

@@ -54,12 +54,21 @@ def test_abi_version_and_strerror(L):
     (dict(batch=70000, max_seq_len=32768), -1),          # B * max_seq_len >= 2^31
     (dict(mode="unified", range_lo=5.0, range_hi=5.0), -1),
     (dict(mode="unified", unified_max=math.inf), -1),
+    (dict(mode="unified_local", range_lo=1.0, range_hi=-1.0), -1),
     (dict(num_sms=-1), -1),
 ])
 def test_plan_rejects_bad_problems(L, kw, code):
     with pytest.raises(binding.DecodeAttnError) as e:
         binding.decode_attn_plan(_prob(**kw), 0)
     assert e.value.code == code
+
+
+def test_plan_rejects_an_unknown_softmax_mode(L):
+    prob = _prob()
+    prob.mode = 3
+    with pytest.raises(binding.DecodeAttnError) as e:
+        binding.decode_attn_plan(prob, 0)
+    assert e.value.code == -1
 
 
 def test_plan_choices_for_the_named_workloads(L):

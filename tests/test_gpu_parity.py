@@ -62,7 +62,7 @@ def gqa32k():
     return _parity.DeviceInputs(inp), _parity.run_oracle(inp)
 
 
-@pytest.mark.parametrize("mode", ["sync", "unified"])
+@pytest.mark.parametrize("mode", ["sync", "unified", "unified_local"])
 def test_gqa_32k_bf16(gqa32k, mode):
     dev, (ref, ref_lse, ref_flag, margin) = gqa32k
     out, lse, flags = _check(dev, ref, ref_lse, mode, where="gqa32k heuristic")
@@ -79,7 +79,7 @@ def paged64():
     return _parity.DeviceInputs(inp), _parity.run_oracle(inp)
 
 
-@pytest.mark.parametrize("mode", ["sync", "unified"])
+@pytest.mark.parametrize("mode", ["sync", "unified", "unified_local"])
 def test_paged_batch64_bf16(paged64, mode):
     dev, (ref, ref_lse, ref_flag, margin) = paged64
     out, lse, flags = _check(dev, ref, ref_lse, mode, where="paged b64 heuristic")
@@ -109,6 +109,14 @@ def test_unified_stress_128k():
     out_s, lse_s, flags_s = _parity.run_gpu(dev, mode="sync")
     _parity.compare(out_s, ref.reshape(out_s.shape), "bf16", where="stress sync")
     assert not flags_s.cpu().numpy().any()
+    # split-local fallback: the same flags, the same results, and no second pass
+    out_l, lse_l, flags_l, st_l = _parity.run_gpu(dev, mode="unified_local", want_stats=True)
+    _parity.compare(out_l, ref.reshape(out_l.shape), "bf16", where="stress unified_local")
+    _parity.compare_lse(lse_l, ref_lse.reshape(lse_l.shape), where="stress unified_local")
+    assert np.array_equal(flags_l.cpu().numpy().ravel(), ref_flag)
+    assert st_l.rows_flagged == int(ref_flag.sum()) and st_l.recompute_launched == 0
+    out_l32, _, _ = _parity.run_gpu(dev, mode="unified_local", out_dtype="f32")
+    _parity.compare(out_l32, ref.reshape(out_l32.shape), "f32", where="stress unified_local f32")
 
 
 # ---- edge sweep: group sizes, head dims, dtypes, layouts, ragged lengths, splits -------------
@@ -127,7 +135,7 @@ def test_edge_sweep(dtype, head_dim, group):
         inp = workloads.generate(wl, offset=group + 3 * head_dim)
         dev = _parity.DeviceInputs(inp)
         ref, ref_lse, _, _ = _parity.run_oracle(inp)
-        for mode in ("sync", "unified"):
+        for mode in ("sync", "unified", "unified_local"):
             ns = (0, 1, 3, 7)[case % 4]
             case += 1
             for od in ((dtype, "f32") if dtype != "f32" else ("f32",)):
@@ -211,20 +219,21 @@ def test_gather_offsets_bit_exact(paged):
 
 
 # ---- overflow detection and synchronised recompute ------------------------------------------
-def test_forced_fallback_every_row():
-    wl = workloads.GQA_32K.replace(name="forced", seq_len=5000, mode="unified")
+@pytest.mark.parametrize("mode", ["unified", "unified_local"])
+def test_forced_fallback_every_row(mode):
+    wl = workloads.GQA_32K.replace(name="forced", seq_len=5000, mode=mode)
     inp = workloads.generate(wl, offset=9)
     dev = _parity.DeviceInputs(inp)
     phi, lo, hi = 0.0, -0.25, 0.25        # N(0,1) logits: every row leaves the range
     ref, ref_lse, ref_flag, margin = _parity.run_oracle(inp, phi=phi, lo=lo, hi=hi)
     assert ref_flag.all() and _parity.margin_ok(margin).all()
-    narrow = binding.DecodeAttention(_parity.problem_for(inp, phi=phi, lo=lo, hi=hi), 0)
+    narrow = binding.DecodeAttention(_parity.problem_for(inp, mode=mode, phi=phi, lo=lo, hi=hi), 0)
     out, lse, flags, st = _parity.run_gpu(dev, want_stats=True, attn=narrow)
     _parity.compare(out, ref.reshape(out.shape), "bf16", where="forced fallback")
     _parity.compare_lse(lse, ref_lse.reshape(lse.shape), where="forced fallback")
     assert flags.cpu().numpy().all() and st.rows_flagged == 32
     # the same workspace then serves an unflagged run (the flagged list was reset)
-    wide = binding.DecodeAttention(_parity.problem_for(inp), 0)
+    wide = binding.DecodeAttention(_parity.problem_for(inp, mode=mode), 0)
     assert wide.workspace_bytes == narrow.workspace_bytes
     wide.workspace = narrow.workspace
     ref2, ref_lse2, _, _ = _parity.run_oracle(inp)
@@ -255,10 +264,11 @@ def test_some_rows_flagged_in_a_paged_batch():
     got_rows = {(int(i) // 32, int(i) % 32) for i in np.flatnonzero(ref_flag)}
     assert flagged <= got_rows and len(got_rows) <= 8   # the planted rows, a few neighbours at most
     assert _parity.margin_ok(margin).all()
-    for od in ("bf16", "f32"):
-        out, lse, flags, st = _parity.run_gpu(dev, out_dtype=od, want_stats=True,
+    for mode, od in (("unified", "bf16"), ("unified", "f32"), ("unified_local", "bf16"),
+                     ("unified_local", "f32")):
+        out, lse, flags, st = _parity.run_gpu(dev, mode=mode, out_dtype=od, want_stats=True,
                                               phi=phi, lo=lo, hi=hi)
-        _parity.compare(out, ref.reshape(out.shape), od, where=f"some rows flagged {od}")
+        _parity.compare(out, ref.reshape(out.shape), od, where=f"some rows flagged {mode} {od}")
         _parity.compare_lse(lse, ref_lse.reshape(lse.shape), where="some rows flagged")
         assert np.array_equal(flags.cpu().numpy().ravel().astype(bool), ref_flag.astype(bool))
         assert st.rows_flagged == int(ref_flag.sum())
@@ -276,9 +286,11 @@ def test_underflow_injection_is_flagged_and_finite():
     dev = _parity.DeviceInputs(inp)
     ref, ref_lse, ref_flag, margin = _parity.run_oracle(inp, phi=0.0, lo=-10.0, hi=10.0)
     assert ref_flag.all() and _parity.margin_ok(margin).all()
-    out, lse, flags = _parity.run_gpu(dev, phi=0.0, lo=-10.0, hi=10.0)
-    _parity.compare(out, ref.reshape(out.shape), "bf16", where="underflow")
-    assert flags.cpu().numpy().all()
+    for mode in ("unified", "unified_local"):
+        out, lse, flags = _parity.run_gpu(dev, mode=mode, phi=0.0, lo=-10.0, hi=10.0)
+        _parity.compare(out, ref.reshape(out.shape), "bf16", where=f"underflow {mode}")
+        _parity.compare_lse(lse, ref_lse.reshape(lse.shape), where=f"underflow {mode}")
+        assert flags.cpu().numpy().all()
 
 
 # ---- validation findings ------------------------------------------------------------------
