@@ -60,6 +60,8 @@ def lib():
         L.oracle_lse_merge_alpha.restype = ctypes.c_int
         L.oracle_lse_merge_alpha.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P, P]
         L.oracle_unified_row.restype = ctypes.c_int
+        L.oracle_logits.argtypes = [ctypes.POINTER(Shape), P, P, P, P, d, P]
+        L.oracle_logits.restype = i64
         L.oracle_unified_row.argtypes = [ctypes.POINTER(Shape), P, P, P, P, P, ctypes.c_int,
                                          ctypes.c_int, d, d, d, d, i64, P, P, P, P]
         _lib = L
@@ -123,6 +125,20 @@ def gather_offsets(shape, block_table, seq_lens):
     if lib().oracle_gather_offsets(ctypes.byref(shape), _ptr(bt), _ptr(sl), _ptr(offs)):
         raise ValueError("oracle_gather_offsets rejected its arguments")
     return offs
+
+
+def logits(shape, q, k, block_table, seq_lens, scale):
+    """Every row's scaled logits in row order (b * H_q + h_q), tokens in order: float64."""
+    dt = _dtype_name(shape)
+    q, k = _bits(q, dt), _bits(k, dt)
+    bt = None if block_table is None else np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    out = np.zeros(int(sl.astype(np.int64).sum()) * shape.num_q_heads, np.float64)
+    n = lib().oracle_logits(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(bt), _ptr(sl), scale,
+                            _ptr(out))
+    if n != out.size:
+        raise ValueError("oracle_logits rejected its arguments")
+    return out
 
 
 def split_partial(shape, q, k, v, block_table, b, h, tokens, scale):

@@ -399,3 +399,23 @@ int oracle_unified_row(const oracle_shape* s, const void* q, const void* k, cons
   free(num_j);
   return rc;
 }
+
+int64_t oracle_logits(const oracle_shape* s, const void* q, const void* k,
+                      const int32_t* block_table, const int32_t* seq_lens, double scale,
+                      double* out) {
+  if (!shape_ok(s) || !q || !k || !seq_lens || !out) return -1;
+  if (s->paged && !block_table) return -1;
+  int64_t n = 0;
+  for (int b = 0; b < s->batch; ++b) {
+    if (seq_lens[b] < 0) return -1;
+    for (int h = 0; h < s->num_q_heads; ++h) {
+      const int kvh = kv_head_of(s, h);
+      for (int64_t t = 0; t < seq_lens[b]; ++t) {
+        const int64_t off = oracle_kv_offset(s, block_table, b, kvh, t);
+        if (off < 0) return -1;
+        out[n++] = logit(s, q, k, b, h, off, scale);
+      }
+    }
+  }
+  return n;
+}

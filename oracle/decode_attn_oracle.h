@@ -102,6 +102,15 @@ int oracle_unified_row(const oracle_shape* s, const void* q, const void* k, cons
                        int64_t split_tokens, double* out, double* lse, uint8_t* flag,
                        int64_t* split_flags);
 
+/* The scaled logits x = scale * q[b,h_q] . k_t of every row, rows in order b * H_q + h_q
+ * and tokens t < seq_lens[b] in order within a row, written to out (which holds
+ * sum_b seq_lens[b] * H_q values): the pre-softmax values whose distribution
+ * "FlashDecoding++" (Fig. 5, "The Overflow and Precision Problem: Choosing phi") reports.
+ * Returns the number written, or -1 on a bad argument or block-table entry. */
+int64_t oracle_logits(const oracle_shape* s, const void* q, const void* k,
+                      const int32_t* block_table, const int32_t* seq_lens, double scale,
+                      double* out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -378,3 +378,48 @@ def test_out_of_pool_block_table_entry_is_rejected():
         oracle.decode_attn(shape, q, k, k, table, np.array([4], np.int32), 1.0)
     out, _, _, _ = oracle.decode_attn(shape, q, k, k, table, np.array([2], np.int32), 1.0)
     assert np.all(out == 1.0)
+
+
+# ---------------------------------------------------------------------------------------
+# The logit values behind the choice of phi ("FlashDecoding++", Fig. 5)
+# ---------------------------------------------------------------------------------------
+def test_logits_of_one_hot_keys_are_single_products():
+    """K row t = c_t e_(t mod d): the scaled logit of head h is scale * c_t * q[h, t mod d]."""
+    rng = np.random.default_rng(31)
+    d, Hq, Hkv, n = 8, 4, 2, 11
+    shape = oracle.make_shape(batch=1, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d, dtype="f32",
+                              max_seq_len=n)
+    q = rng.standard_normal((1, Hq, d)).astype(np.float32)
+    c = rng.standard_normal(n).astype(np.float32)
+    k = np.zeros((1, n, Hkv, d), np.float32)
+    for t in range(n):
+        k[0, t, :, t % d] = c[t]
+    x = oracle.logits(shape, q, k, None, np.array([n], np.int32), 0.5)
+    assert x.shape == (Hq * n,)
+    for h in range(Hq):
+        for t in range(n):
+            assert x[h * n + t] == 0.5 * float(c[t]) * float(q[0, h, t % d])
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_logits_agree_with_the_attention_oracle(paged):
+    """Each row's logits reproduce the (separately pinned) attention oracle: their
+    log-sum-exp is its lse, row by row, in the documented order; in the paged case that
+    also ties them to the block-table gather the attention oracle uses."""
+    rng = np.random.default_rng(32)
+    lens = [5, 0, 23, 9]
+    shape, q, k, v, table, sl = _tiny_case(rng, "bf16", paged, 4, 4, 2, 16, lens, 4, False)
+    x = oracle.logits(shape, q, k, table, sl, 0.3)
+    out, lse, _, _ = oracle.decode_attn(shape, q, k, v, table, sl, 0.3)
+    at = 0
+    for b, n in enumerate(lens):
+        for h in range(4):
+            r = b * 4 + h
+            xs = x[at:at + n]
+            at += n
+            if n == 0:
+                assert lse[r] == -math.inf
+                continue
+            m = xs.max()
+            assert abs(m + math.log(np.exp(xs - m).sum()) - lse[r]) < 1e-12
+    assert at == x.size
