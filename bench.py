@@ -51,6 +51,9 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--op", default="attention", choices=["attention", "logit_histogram"],
+                    help="attention: the decode step (default); logit_histogram: the phi "
+                         "calibration pass over the same workload")
     return ap.parse_args()
 
 
@@ -89,10 +92,10 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload_name):
-    """dram read+write bytes per split-kernel launch from the committed ncu summary, or None
+def profiled_traffic(workload_name, kernel="split_kernel"):
+    """dram read+write bytes per launch of `kernel` from the committed ncu summary, or None
     when the summary is missing or was taken on different kernel sources."""
-    path = os.path.join(ROOT, "profiles", f"split_kernel_{workload_name}.md")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload_name}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -248,15 +251,10 @@ def run_ours(args):
         attn.run(dev.q, dev.k, dev.v, dev.bt, dev.sl, wl.scale, args.num_splits, out=out,
                  out_lse=lse, row_flags=flags, stream=stream, split_events=split_events)
 
-    # correctness guard on this very launch configuration: sampled rows against the oracle
     for _ in range(max(3, args.warmup)):
         flush()
         step()
     torch.cuda.synchronize()
-    sample_rows = list(range(0, B * H, max(1, (B * H) // 8)))[:8]
-    ref, ref_lse, _, _ = _parity.run_oracle(inp, rows=sample_rows)
-    got = out.reshape(B * H, d)[sample_rows]
-    _parity.compare(got, ref, wl.out_dtype, where="bench guard")
 
     # ---- timed region: whole steps ----
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -377,14 +375,16 @@ def run_ours(args):
         "wall_s_timed": round(t_wall, 3),
     }
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds, out)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
 
 
-def cpu_baseline(inp, seconds):
-    """The float64 CPU oracle, as it stands, on this host's cores over the same inputs."""
+def cpu_baseline(inp, seconds, out=None):
+    """The float64 CPU oracle, as it stands, on this host's cores over the same inputs. When
+    `out` (the GPU result of the timed launch configuration on these inputs) is given, the
+    oracle's result also checks it, within the parity tolerance."""
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     import _parity
     import oracle
@@ -393,14 +393,17 @@ def cpu_baseline(inp, seconds):
     t0 = time.perf_counter()
     n = 0
     while True:
-        _parity.run_oracle(inp, nthreads=threads)
+        ref = _parity.run_oracle(inp, nthreads=threads)[0]
         n += 1
         if time.perf_counter() - t0 >= seconds:
             break
     dt = (time.perf_counter() - t0) / n
+    if out is not None:
+        _parity.compare(out, ref, inp.wl.out_dtype, where="bench output vs oracle")
     return {"value": round(inp.kv_bytes() / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
             "kind": "oracle", "ms_per_step": round(dt * 1e3, 2),
-            "sample": f"the whole workload ({rows} query rows, every token), {n} passes"}
+            "sample": f"the whole workload ({rows} query rows, every token), {n} passes",
+            "checked_gpu_output": out is not None}
 
 
 def run_reference(args):
@@ -449,10 +452,161 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+HIST_LO, HIST_HI, HIST_BINS = -16.0, 16.0, 4096
+
+
+def oracle_histogram(inp):
+    """Histogram of the oracle's float64 logits, slots as the library lays them out."""
+    import numpy as np
+    import oracle
+    from decode_attention_attn_gb300 import workloads
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import _parity
+    bt = None if inp.block_table is None else inp.block_table.numpy()
+    x = oracle.logits(_parity.oracle_shape(inp), workloads.bits(inp.q), workloads.bits(inp.k_cache),
+                      bt, inp.seq_lens.numpy(), inp.wl.scale)
+    w = (HIST_HI - HIST_LO) / HIST_BINS
+
+    def slots(v):
+        i = np.floor((v - HIST_LO) / w)
+        return np.where(i < 0, 0, np.where(i >= HIST_BINS, HIST_BINS + 1, i + 1)).astype(np.int64)
+    tol = 2e-5 * (1.0 + np.abs(x))
+    edge = int(np.count_nonzero(slots(x - tol) != slots(x + tol)))
+    return np.bincount(slots(x), minlength=HIST_BINS + 2), edge
+
+
+def run_histogram(args):
+    """The calibration pass (decode_attn_logit_histogram) timed like the decode step: one
+    launch per step over the workload's K, L2 flushed before each step."""
+    import numpy as np
+    import torch
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import _parity
+    from decode_attention_attn_gb300 import binding, workloads
+
+    rank, world, local = dist_env()
+    if world > 1:
+        print(json.dumps({"op": "logit_histogram", "unavailable": "one GPU only"}))
+        return
+    torch.cuda.set_device(local)
+    wl = workloads.get(args.workload)
+    inp = workloads.generate(wl)
+    k_bytes = inp.kv_bytes() // 2
+    dev = _parity.DeviceInputs(inp)
+    attn = binding.DecodeAttention(_parity.problem_for(inp, mode="sync"), 0)
+    stream = torch.cuda.current_stream()
+    flush = L2Flush(f"cuda:{local}")
+    counts = torch.zeros(HIST_BINS + 2, dtype=torch.int64, device=f"cuda:{local}")
+
+    def step():
+        binding.decode_attn_logit_histogram(
+            attn.plan, dev.q.data_ptr(), dev.k.data_ptr(),
+            None if dev.bt is None else dev.bt.data_ptr(), dev.sl.data_ptr(), wl.scale,
+            HIST_LO, HIST_HI, HIST_BINS, counts.data_ptr(), stream.cuda_stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush()
+        step()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    torch.cuda.synchronize()
+    sampler.start()
+    for i in range(args.steps):
+        flush()
+        torch.cuda._sleep(HOST_AHEAD_CYCLES)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps
+
+    # end to end: pinned q, K, lengths and table in; the counts out
+    e2e = None
+    hq, hk, hsl = inp.q.pin_memory(), inp.k_cache.pin_memory(), inp.seq_lens.pin_memory()
+    hbt = None if inp.block_table is None else inp.block_table.pin_memory()
+    hcounts = torch.empty(counts.shape, dtype=counts.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hsl) + ((hbt,) if hbt is not None else ()))
+    d2h = hcounts.numel() * hcounts.element_size()
+    e_steps = 1 if args.no_e2e else max(5, min(args.steps, 20))
+    es = [torch.cuda.Event(enable_timing=True) for _ in range(e_steps)]
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(e_steps)]
+    for i in range(e_steps):   # (one untimed pass with --no-e2e: the counts the check reads)
+        es[i].record(stream)
+        dev.q.copy_(hq, non_blocking=True)
+        dev.k.copy_(hk, non_blocking=True)
+        dev.sl.copy_(hsl, non_blocking=True)
+        if hbt is not None:
+            dev.bt.copy_(hbt, non_blocking=True)
+        counts.zero_()
+        step()
+        hcounts.copy_(counts, non_blocking=True)
+        ee[i].record(stream)
+        stream.synchronize()
+    if not args.no_e2e:
+        e2e_ms = sum(s.elapsed_time(e) for s, e in zip(es, ee)) / e_steps
+        e2e = {"value": round(k_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e2e_ms, 4)}
+
+    # the oracle's logits plus a numpy histogram, timed on the host cores; its result also
+    # checks the last GPU histogram (one step's, from the e2e loop): slots may differ only by
+    # logits within the fp32 error of a bin edge
+    cpu = None
+    if not args.no_cpu_baseline:
+        t0 = time.perf_counter()
+        n = 0
+        while n == 0 or time.perf_counter() - t0 < args.cpu_seconds:
+            ref, edge = oracle_histogram(inp)
+            n += 1
+        cpu_dt = (time.perf_counter() - t0) / n
+        diff = int(np.abs(hcounts.numpy() - ref).sum())
+        assert diff <= 2 * edge, f"histogram differs from the oracle's by {diff} (> 2 x {edge})"
+        cpu = {"value": round(k_bytes / cpu_dt / 1e9, 4), "unit": "GB/s", "cores": 1,
+               "kind": "oracle", "ms_per_step": round(cpu_dt * 1e3, 2),
+               "sample": f"the whole workload (every logit, float64) plus a numpy histogram, "
+                         f"{n} passes", "checked_gpu_output": True}
+
+    peak, peak_kind = measured_peaks()
+    achieved = k_bytes / (ms * 1e-3) / 1e9
+    line = {
+        "op": "logit_histogram",
+        "metric": "logit-histogram K-read GB/s (phi calibration pass)",
+        "value": round(achieved, 2),
+        "unit": "GB/s",
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "us_per_step": round(ms * 1e3, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded N(0,1), workloads.py recipe)",
+        "config": {"workload": wl.name, "k_bytes_per_step": k_bytes,
+                   "bins": HIST_BINS, "range": [HIST_LO, HIST_HI],
+                   "l2": f"flushed before every timed step: {FLUSH_BYTES >> 20} MiB written, then {FLUSH_BYTES >> 20} MiB of another buffer read"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peak_kind} hbm_gbs", "kernel": "logit_histogram_kernel",
+                     "traffic": profiled_traffic(wl.name, "logit_histogram")},
+        "clocks": clocks,
+        "gpu_launches": args.steps,
+        "e2e": e2e,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.op == "logit_histogram":
+        run_histogram(args)
     else:
         run_ours(args)
 

@@ -18,7 +18,10 @@ DA_F32, DA_F16, DA_BF16 = 0, 1, 2
 DA_SOFTMAX_SYNC, DA_SOFTMAX_UNIFIED, DA_SOFTMAX_UNIFIED_LOCAL = 0, 1, 2
 ERRORS = {0: "DA_OK", -1: "DA_ERR_INVALID_ARG", -2: "DA_ERR_UNSUPPORTED",
           -3: "DA_ERR_WORKSPACE_TOO_SMALL", -4: "DA_ERR_BAD_BLOCK_TABLE", -5: "DA_ERR_CUDA",
-          -6: "DA_ERR_DEVICE_TIMEOUT", -7: "DA_ERR_BAD_SEQ_LEN"}
+          -6: "DA_ERR_DEVICE_TIMEOUT", -7: "DA_ERR_BAD_SEQ_LEN", -8: "DA_ERR_HISTOGRAM_RANGE",
+          -9: "DA_ERR_RANGE_TOO_WIDE"}
+DA_ERR_RANGE_TOO_WIDE = -9
+MAX_HIST_BINS = 32768
 DTYPE_CODES = {"f32": DA_F32, "f16": DA_F16, "bf16": DA_BF16}
 MODE_CODES = {"sync": DA_SOFTMAX_SYNC, "unified": DA_SOFTMAX_UNIFIED,
               "unified_local": DA_SOFTMAX_UNIFIED_LOCAL}
@@ -126,6 +129,12 @@ def lib():
                                              P, P, P, ctypes.POINTER(da_stats)]
         L.decode_attn_check_status.argtypes = [P, P, P]
         L.decode_attn_debug_gather.argtypes = [P, P, P, P, P]
+        L.decode_attn_logit_histogram.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_float,
+                                                  ctypes.c_float, ctypes.c_int, P, P]
+        F = ctypes.POINTER(ctypes.c_float)
+        L.decode_attn_choose_phi.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), ctypes.c_int,
+                                             ctypes.c_float, ctypes.c_float, ctypes.c_double,
+                                             ctypes.c_float, F, F, F]
         L.decode_attn_destroy.argtypes = [P]
         L.decode_attn_destroy.restype = None
         L.decode_attn_strerror.argtypes = [ctypes.c_int]
@@ -134,7 +143,8 @@ def lib():
         for name in ("decode_attn_plan", "decode_attn_plan_info", "decode_attn_workspace_init",
                      "decode_attn_run", "decode_attn_run_ex", "decode_attn_run_static",
                      "decode_attn_check_status",
-                     "decode_attn_debug_gather",
+                     "decode_attn_debug_gather", "decode_attn_logit_histogram",
+                     "decode_attn_choose_phi",
                      "decode_attn_abi_version"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -226,6 +236,33 @@ def decode_attn_debug_gather(plan, block_table: Optional[int], seq_lens: int, of
                              stream: int = 0):
     _check(lib().decode_attn_debug_gather(plan, block_table or None, seq_lens, offsets_out,
                                           stream or None), "decode_attn_debug_gather")
+
+
+def decode_attn_logit_histogram(plan, q: int, k_cache: int, block_table: Optional[int],
+                                seq_lens: int, scale: float, lo: float, hi: float, nbins: int,
+                                counts: int, stream: int = 0):
+    """Accumulate the histogram of one step's scaled logits into the device uint64 buffer
+    `counts` ([nbins + 2]: below lo, the nbins bins of [lo, hi), at or above hi)."""
+    _check(lib().decode_attn_logit_histogram(plan, q, k_cache, block_table or None, seq_lens,
+                                             scale, lo, hi, nbins, counts, stream or None),
+           "decode_attn_logit_histogram")
+
+
+def decode_attn_choose_phi(counts, lo: float, hi: float, coverage: float = 0.9999,
+                           max_width: float = float("inf")):
+    """(phi, x_lo, x_hi, applies) from a host histogram (a sequence of nbins + 2 counts).
+    applies is False when the covered range is wider than max_width (the unified max should
+    not be used for this data); other failures raise."""
+    n = len(counts) - 2
+    if n < 1:
+        raise ValueError("a histogram holds at least one bin and the two outer counts")
+    arr = (ctypes.c_ulonglong * len(counts))(*[int(c) for c in counts])
+    phi, x_lo, x_hi = ctypes.c_float(), ctypes.c_float(), ctypes.c_float()
+    rc = lib().decode_attn_choose_phi(arr, n, lo, hi, coverage, max_width, ctypes.byref(phi),
+                                      ctypes.byref(x_lo), ctypes.byref(x_hi))
+    if rc not in (0, DA_ERR_RANGE_TOO_WIDE):
+        _check(rc, "decode_attn_choose_phi")
+    return phi.value, x_lo.value, x_hi.value, rc == 0
 
 
 def decode_attn_destroy(plan):

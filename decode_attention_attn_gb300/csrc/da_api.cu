@@ -43,6 +43,145 @@ __global__ void debug_gather_kernel(const __grid_constant__ Params p) {
     p.debug_offsets[i] = off;
   }
 }
+
+// ---- logit histogram: the calibration pass behind the choice of phi ----------------------
+// "FlashDecoding++", Fig. 5 and "The Overflow and Precision Problem: Choosing phi": the
+// distribution of the scaled logits x = scale * q[b, h] . K[b, t, h / G] over every row and
+// token of a step, from which phi and the covered range are read. Not on the attention path:
+// a plain memory-bound pass over K (one read of every used K row; q from L2 into registers).
+
+constexpr int kHistThreads = 256;
+constexpr int kHistWarps = kHistThreads / 32;
+constexpr int kHistItemTokens = 64;   // tokens of one (b, kv head) per warp work item
+
+// Bin of x: i = floor((x - lo) * inv_w) in fp32 gives counts[1 + i] for 0 <= i < nbins,
+// counts[0] below lo, counts[nbins + 1] at or above the top edge and for NaN.
+__device__ __forceinline__ int hist_bin(float x, float lo, float inv_w, int nbins) {
+  if (x != x) return nbins + 1;
+  if (x < lo) return 0;
+  const float f = floorf((x - lo) * inv_w);
+  return f >= (float)nbins ? nbins + 1 : 1 + (int)f;
+}
+
+// One warp per work item (64 tokens of one sequence and KV head); a K row is split over C
+// lanes, 16 bytes each, so a warp reads R = 32 / C rows per load and U loads per lane are in
+// flight before any arithmetic. The pass is latency-bound per warp, so the number of resident
+// warps matters more than U: registers are capped for 4 blocks of 8 warps per SM (2-3 for
+// G = 8, whose q takes up to 64 registers); on the bf16 GQA shapes U = 2 at 4 blocks streams
+// K 1.5x faster than U = 8 at 2. The G query heads of the KV head sit in registers as fp32
+// pairs. The C lanes' G partial dot products are summed by a transposing butterfly: each of
+// the first log2 G exchange steps hands half of a lane's heads to its partner, so a row costs
+// G - 1 + log2(C / G) shuffles instead of G log2 C; afterwards the top log2 G bits of the
+// lane's index within its row name the head it holds the sum for.
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kHistThreads, G == 8 ? (sizeof(T) == 4 ? 3 : 2) : 4)
+    logit_histogram_kernel(const __grid_constant__ Params p, const T* __restrict__ kc,
+                           float scale, float lo, float inv_w, int nbins,
+                           unsigned long long* __restrict__ counts) {
+  extern __shared__ unsigned hist[];   // [nbins + 2]
+  constexpr int EPC = Elem<T>::kPerChunk;   // elements per 16-byte chunk
+  constexpr int NP = EPC / 2;               // fp32 pairs per chunk
+  constexpr int C = D / EPC;                // lanes per K row: 8, 16 or 32
+  constexpr int R = 32 / C;                 // K rows per warp load
+  constexpr int U = 2;                      // loads in flight per lane
+  constexpr int LG = G == 1 ? 0 : (G == 2 ? 1 : (G == 4 ? 2 : 3));
+  static_assert(G <= C, "a row's lanes must cover its heads");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = lane / C, c = lane % C;
+  const bool binner = (c % (C / G)) == 0;   // one lane of the C / G holding each head's sum
+
+  for (int i = threadIdx.x; i < nbins + 2; i += kHistThreads) hist[i] = 0;
+  __syncthreads();
+
+  const int chunks = (p.capacity + kHistItemTokens - 1) / kHistItemTokens;
+  const long long items = (long long)p.batch * p.hkv * chunks;
+  for (long long it = (long long)blockIdx.x * kHistWarps + warp; it < items;
+       it += (long long)gridDim.x * kHistWarps) {
+    const int ch = (int)(it % chunks);
+    const int kvh = (int)((it / chunks) % p.hkv);
+    const int b = (int)(it / chunks / p.hkv);
+    const int raw = p.seq_lens[b];
+    const int n = raw < 0 ? 0 : (raw > p.capacity ? p.capacity : raw);
+    const int t0 = ch * kHistItemTokens;
+    if (t0 >= n) continue;                  // the same for the whole warp
+    const int t1 = min(n, t0 + kHistItemTokens);
+
+    f32x2 qp[G][NP];
+    const T* qg = static_cast<const T*>(p.q) + ((long long)b * p.hq + (long long)kvh * G) * D;
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+      Elem<T>::to_pairs(__ldg(reinterpret_cast<const uint4*>(qg + g * D) + c), qp[g]);
+
+    for (int tb = t0; tb < t1; tb += R * U) {
+      uint4 kr[U];
+      bool ok[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int t = tb + u * R + sub;
+        int z = -1;
+        if (t < t1) {
+          const int entry =
+              p.paged ? p.block_table[(long long)b * p.max_blocks + t / p.page_size] : 0;
+          z = token_row(p, b, t, entry);
+        }
+        ok[u] = z >= 0;
+        kr[u] = make_uint4(0, 0, 0, 0);
+        if (ok[u])
+          kr[u] = __ldg(reinterpret_cast<const uint4*>(kc + ((long long)z * p.hkv + kvh) * D) + c);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        f32x2 kf[NP];
+        Elem<T>::to_pairs(kr[u], kf);
+        float v[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          f32x2 a = f2_mul(qp[g][0], kf[0]);
+#pragma unroll
+          for (int j = 1; j < NP; ++j) f2_fma(a, qp[g][j], kf[j]);
+          float x0, x1;
+          f2_unpack(a, x0, x1);
+          v[g] = x0 + x1;
+        }
+#pragma unroll
+        for (int s = 0; s < LG; ++s) {          // transposing steps: offsets C/2, C/4, ...
+          const int o = C >> (s + 1);
+          const int half = G >> (s + 1);
+          const bool upper = (lane & o) != 0;
+#pragma unroll
+          for (int i = 0; i < half; ++i) {
+            const float send = upper ? v[i] : v[i + half];
+            const float keep = upper ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+          }
+        }
+#pragma unroll
+        for (int o = C >> (LG + 1); o > 0; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+        if (ok[u] && binner) atomicAdd(&hist[hist_bin(scale * v[0], lo, inv_w, nbins)], 1u);
+      }
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < nbins + 2; i += kHistThreads)
+    if (hist[i]) atomicAdd(&counts[i], (unsigned long long)hist[i]);
+}
+
+template <typename T, int D>
+const void* histogram_kernel_for_d(int G) {
+  switch (G) {
+    case 1: return reinterpret_cast<const void*>(&logit_histogram_kernel<T, D, 1>);
+    case 2: return reinterpret_cast<const void*>(&logit_histogram_kernel<T, D, 2>);
+    case 4: return reinterpret_cast<const void*>(&logit_histogram_kernel<T, D, 4>);
+    case 8: return reinterpret_cast<const void*>(&logit_histogram_kernel<T, D, 8>);
+    default: return nullptr;
+  }
+}
+
+template <typename T>
+const void* histogram_kernel_for(int D, int G) {
+  return D == 64 ? histogram_kernel_for_d<T, 64>(G)
+                 : (D == 128 ? histogram_kernel_for_d<T, 128>(G) : nullptr);
+}
 }  // namespace da
 
 using namespace da;
@@ -270,6 +409,10 @@ const char* decode_attn_strerror(int code) {
     case DA_ERR_CUDA: return g_cuda_error.empty() ? "CUDA error" : g_cuda_error.c_str();
     case DA_ERR_DEVICE_TIMEOUT: return "a device pipeline wait ran out of time";
     case DA_ERR_BAD_SEQ_LEN: return "a sequence length is negative or above the cache capacity";
+    case DA_ERR_HISTOGRAM_RANGE:
+      return "a tail of the requested coverage lies outside the histogram's range";
+    case DA_ERR_RANGE_TOO_WIDE:
+      return "the covered logit range is wider than allowed: use DA_SOFTMAX_SYNC";
     default: return "unknown error code";
   }
 }
@@ -593,6 +736,85 @@ int decode_attn_debug_gather(const da_plan* plan, const int32_t* block_table,
                         static_cast<cudaStream_t>(cuda_stream)>>>(kp);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? DA_OK : cuda_fail(e, "launching the debug gather kernel");
+}
+
+int decode_attn_logit_histogram(const da_plan* plan, const void* q, const void* k_cache,
+                                const int32_t* block_table, const int32_t* seq_lens,
+                                float scale, float lo, float hi, int nbins,
+                                unsigned long long* counts, void* cuda_stream) {
+  if (!plan || !q || !k_cache || !seq_lens || !counts) return DA_ERR_INVALID_ARG;
+  const da_plan& pl = *plan;
+  if (pl.prob.paged ? !block_table : block_table != nullptr) return DA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(seq_lens, 4) ||
+      !aligned(counts, 8) || (block_table && !aligned(block_table, 4)))
+    return DA_ERR_INVALID_ARG;
+  if (nbins < 1 || nbins > DECODE_ATTN_MAX_HIST_BINS) return DA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !std::isfinite(lo) || !std::isfinite(hi) || !(lo < hi))
+    return DA_ERR_INVALID_ARG;
+  const float inv_w = (float)((double)nbins / ((double)hi - (double)lo));
+  if (!std::isfinite(inv_w) || !(inv_w > 0.f)) return DA_ERR_INVALID_ARG;
+
+  const void* fn = nullptr;
+  switch (pl.prob.qkv_dtype) {
+    case DA_F32: fn = histogram_kernel_for<float>(pl.prob.head_dim, pl.group); break;
+    case DA_F16: fn = histogram_kernel_for<__half>(pl.prob.head_dim, pl.group); break;
+    default: fn = histogram_kernel_for<__nv_bfloat16>(pl.prob.head_dim, pl.group); break;
+  }
+  if (!fn) return DA_ERR_UNSUPPORTED;
+  const size_t smem = ((size_t)nbins + 2) * 4;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(histogram smem)");
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kHistThreads, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+  const long long items = (long long)pl.prob.batch * pl.prob.num_kv_heads *
+                          ((pl.capacity + kHistItemTokens - 1) / kHistItemTokens);
+  const long long blocks = (items + kHistWarps - 1) / kHistWarps;
+  const int grid =
+      (int)std::max(1ll, std::min(blocks, (long long)pl.num_sms * std::max(1, per_sm)));
+
+  Params kp;
+  fill_common(pl, kp, block_table, seq_lens, nullptr);
+  kp.q = q;
+  void* args[7] = {&kp, &k_cache, &scale, &lo, const_cast<float*>(&inv_w), &nbins, &counts};
+  e = cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(kHistThreads), args, smem,
+                       static_cast<cudaStream_t>(cuda_stream));
+  return e == cudaSuccess ? DA_OK : cuda_fail(e, "launching the logit histogram kernel");
+}
+
+int decode_attn_choose_phi(const unsigned long long* counts, int nbins, float lo, float hi,
+                           double coverage, float max_width, float* phi, float* x_lo,
+                           float* x_hi) {
+  if (!counts || !phi || !x_lo || !x_hi || nbins < 1) return DA_ERR_INVALID_ARG;
+  if (!(coverage > 0.0 && coverage <= 1.0) || !(max_width > 0.f)) return DA_ERR_INVALID_ARG;
+  if (!std::isfinite(lo) || !std::isfinite(hi) || !(lo < hi)) return DA_ERR_INVALID_ARG;
+  double total = 0.0;
+  for (int i = 0; i < nbins + 2; ++i) total += (double)counts[i];
+  if (total == 0.0) return DA_ERR_INVALID_ARG;
+  // At most `tail` values may lie outside the range on each side, so that the range holds
+  // at least the fraction `coverage` of them.
+  const double tail = std::floor((1.0 - coverage) * total / 2.0);
+  const double under = (double)counts[0], over = (double)counts[nbins + 1];
+  if (under > tail || over > tail) return DA_ERR_HISTOGRAM_RANGE;
+  int first = 0;                 // first kept bin
+  double below = under;
+  while (first < nbins && below + (double)counts[1 + first] <= tail)
+    below += (double)counts[1 + first++];
+  int last = nbins - 1;          // last kept bin
+  double above = over;
+  while (last >= 0 && above + (double)counts[1 + last] <= tail)
+    above += (double)counts[1 + last--];
+  // first <= last: otherwise every value would be among the <= 2 * tail < total dropped.
+  const double w = ((double)hi - (double)lo) / nbins;
+  const double e_lo = (double)lo + first * w, e_hi = (double)lo + (last + 1) * w;
+  float f_lo = (float)e_lo, f_hi = (float)e_hi;   // rounded outwards to fp32
+  if ((double)f_lo > e_lo) f_lo = std::nextafter(f_lo, -INFINITY);
+  if ((double)f_hi < e_hi) f_hi = std::nextafter(f_hi, INFINITY);
+  *x_lo = f_lo;
+  *x_hi = f_hi;
+  *phi = f_lo;   // phi = the lower bound of the covered range
+  return (double)f_hi - (double)f_lo > (double)max_width ? DA_ERR_RANGE_TOO_WIDE : DA_OK;
 }
 
 }  // extern "C"

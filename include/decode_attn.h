@@ -45,6 +45,9 @@ extern "C" {
 
 #define DECODE_ATTN_ABI_VERSION 1
 
+/* Largest bin count decode_attn_logit_histogram accepts. */
+#define DECODE_ATTN_MAX_HIST_BINS 32768
+
 typedef enum { DA_F32 = 0, DA_F16 = 1, DA_BF16 = 2 } da_dtype;
 
 /* DA_SOFTMAX_SYNC: each split runs the online-softmax recurrence with its running
@@ -76,7 +79,9 @@ enum {
   DA_ERR_BAD_BLOCK_TABLE = -4,      /* validate: a used block-table entry outside the pool */
   DA_ERR_CUDA = -5,                 /* a CUDA runtime / driver call failed */
   DA_ERR_DEVICE_TIMEOUT = -6,       /* validate: a device pipeline wait ran out of time */
-  DA_ERR_BAD_SEQ_LEN = -7           /* validate: seq_lens[b] < 0 or above the capacity */
+  DA_ERR_BAD_SEQ_LEN = -7,          /* validate: seq_lens[b] < 0 or above the capacity */
+  DA_ERR_HISTOGRAM_RANGE = -8,      /* choose_phi: a coverage tail lies outside [lo, hi) */
+  DA_ERR_RANGE_TOO_WIDE = -9        /* choose_phi: covered range wider than max_width */
 };
 
 typedef struct {
@@ -257,6 +262,59 @@ int decode_attn_check_status(const da_plan* plan, void* workspace, void* cuda_st
  * block-table entry outside the pool. Enqueued on `stream`. Errors: INVALID_ARG, CUDA. */
 int decode_attn_debug_gather(const da_plan* plan, const int32_t* block_table,
                              const int32_t* seq_lens, int64_t* offsets_out, void* cuda_stream);
+
+/* ---- Calibration: choosing phi from the logits of a step --------------------------------
+ * "FlashDecoding++: Faster Large Language Model Inference on GPUs", "The Overflow and
+ * Precision Problem: Choosing phi" and Fig. 5: the logits of a model's attention rows stay in
+ * a narrow range, profiled as a histogram over many inputs; phi is set to the lower end of
+ * the range that holds more than 99.99% of them, and where that range is too wide (OPT-6.7B
+ * in Fig. 5) the unified max is not used. These two calls run that profile on the caller's
+ * own steps: accumulate one histogram over as many steps as wanted, then read phi off it.
+ * Neither is on the attention path. */
+
+/* Histogram of the scaled logits x = scale * q[b,h] . k_t of one step, over every query head
+ * h and every token t < seq_lens[b] of every sequence b, read through the plan's layout
+ * (contiguous or block table, GQA mapping kv_head = h / G) as decode_attn_run reads them.
+ *   plan: any plan of the problem shape; its softmax mode, phi and range are not used.
+ *   q, k_cache, block_table, seq_lens, scale: as for decode_attn_run (device; k_cache
+ *     16-byte aligned). v_cache is not read.
+ *   lo, hi, nbins: nbins equal bins over [lo, hi), lo < hi finite, 1 <= nbins <=
+ *     DECODE_ATTN_MAX_HIST_BINS. x falls in bin i = floor((x - lo) * (nbins / (hi - lo))),
+ *     evaluated in fp32 from an fp32 dot product, so a logit within a few fp32 ulps of a bin
+ *     edge may fall on either side of it.
+ *   counts: device uint64 [nbins + 2], 8-byte aligned, ACCUMULATED into (zero it before the
+ *     first step): counts[0] = values below lo, counts[1 + i] = bin i, counts[nbins + 1] =
+ *     values at or above the top edge, and NaN.
+ * A token whose block-table entry lies outside the pool, and tokens past the capacity, are
+ * not counted: the counts then sum to less than H_q * sum_b min(seq_lens[b], capacity), which
+ * the caller can check. Enqueued on `stream`; not synchronised.
+ * Errors: INVALID_ARG (null or misaligned pointer, bad range or bin count), UNSUPPORTED,
+ * CUDA. */
+int decode_attn_logit_histogram(const da_plan* plan, const void* q, const void* k_cache,
+                                const int32_t* block_table, const int32_t* seq_lens,
+                                float scale, float lo, float hi, int nbins,
+                                unsigned long long* counts, void* cuda_stream);
+
+/* Host only: phi and the covered logit range from a histogram laid out as above.
+ *   counts: HOST uint64 [nbins + 2]; nbins, lo, hi: those the histogram was taken with.
+ *   coverage: the fraction of values the range must hold, in (0, 1] (0.9999 in Fig. 5).
+ *     At most floor((1 - coverage) * total / 2) values are left out on each side, whole bins
+ *     at a time, so the range is bin-aligned and holds at least that fraction.
+ *   max_width: the widest covered range (x_hi - x_lo) for which the unified max is used.
+ *   x_lo, x_hi (out): the covered range, bin edges rounded outwards to fp32.
+ *   phi (out): x_lo, the pages' choice (the lower bound: a value below it underflows
+ *     harmlessly, none in range overflows). With it, the in-range interval on x - phi of
+ *     the covered values is [0, x_hi - x_lo]; da_problem's [range_lo, range_hi] may be set
+ *     wider, to what fp32 tolerates, so that only values that would lose precision or
+ *     overflow flag their rows.
+ * Errors: INVALID_ARG (null pointer, empty histogram, bad coverage, range or max_width);
+ * HISTOGRAM_RANGE (more than a tail's share of values lies below lo or at or above hi:
+ * repeat the histogram over a wider [lo, hi); outputs not written); RANGE_TOO_WIDE (outputs
+ * written, but x_hi - x_lo > max_width: the unified max does not apply to this data, use
+ * DA_SOFTMAX_SYNC, as Fig. 5 does for OPT-6.7B). Touches no device. */
+int decode_attn_choose_phi(const unsigned long long* counts, int nbins, float lo, float hi,
+                           double coverage, float max_width, float* phi, float* x_lo,
+                           float* x_hi);
 
 void decode_attn_destroy(da_plan* plan);
 
