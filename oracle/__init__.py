@@ -15,7 +15,7 @@ import numpy as np
 
 from . import build as _build
 
-DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2}
+DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2, "e4m3": 3}
 
 _lib = None
 
@@ -32,6 +32,9 @@ class Shape(ctypes.Structure):
         ("max_seq_len", ctypes.c_int),
         ("num_physical_blocks", ctypes.c_int),
         ("dtype", ctypes.c_int),
+        ("kv_e4m3", ctypes.c_int),
+        ("k_scale", ctypes.c_double),
+        ("v_scale", ctypes.c_double),
     ]
 
 
@@ -74,20 +77,31 @@ def _ptr(a):
 
 def _bits(a, dtype):
     a = np.ascontiguousarray(a)
-    want = np.float32 if dtype == "f32" else np.uint16
+    want = {"f32": np.float32, "e4m3": np.uint8}.get(dtype, np.uint16)
     if a.dtype != want:
         raise TypeError(f"oracle expects {np.dtype(want).name} storage for {dtype}, got {a.dtype}")
     return a
 
 
 def make_shape(*, batch, num_q_heads, num_kv_heads, head_dim, dtype, paged=False, page_size=16,
-               max_blocks_per_seq=0, max_seq_len=0, num_physical_blocks=0):
+               max_blocks_per_seq=0, max_seq_len=0, num_physical_blocks=0, kv_dtype=None,
+               k_scale=1.0, v_scale=1.0):
+    """dtype: q's storage (and K / V's, unless kv_dtype="e4m3": an FP8 cache whose codes
+    stand for code * k_scale and code * v_scale)."""
+    if kv_dtype not in (None, dtype, "e4m3"):
+        raise ValueError("K / V are stored like q or as e4m3")
+    fp8 = kv_dtype == "e4m3"
     return Shape(batch, num_q_heads, num_kv_heads, head_dim, int(bool(paged)), page_size,
-                 max_blocks_per_seq, max_seq_len, num_physical_blocks, DTYPE_CODES[dtype])
+                 max_blocks_per_seq, max_seq_len, num_physical_blocks, DTYPE_CODES[dtype],
+                 int(fp8), k_scale if fp8 else 0.0, v_scale if fp8 else 0.0)
 
 
 def _dtype_name(shape):
     return {v: k for k, v in DTYPE_CODES.items()}[shape.dtype]
+
+
+def _kv_dtype_name(shape):
+    return "e4m3" if shape.kv_e4m3 else _dtype_name(shape)
 
 
 def load(dtype, arr, index):
@@ -98,8 +112,8 @@ def load(dtype, arr, index):
 def decode_attn(shape, q, k, v, block_table, seq_lens, scale, phi=0.0, range_lo=-math.inf,
                 range_hi=math.inf, rows=None, nthreads=1):
     """Returns (out [n, d] float64, lse [n], row_flag [n] uint8, margin [n])."""
-    dt = _dtype_name(shape)
-    q, k, v = _bits(q, dt), _bits(k, dt), _bits(v, dt)
+    dt, kdt = _dtype_name(shape), _kv_dtype_name(shape)
+    q, k, v = _bits(q, dt), _bits(k, kdt), _bits(v, kdt)
     bt = None if block_table is None else np.ascontiguousarray(block_table, dtype=np.int32)
     sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
     rows_a = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
@@ -129,8 +143,8 @@ def gather_offsets(shape, block_table, seq_lens):
 
 def logits(shape, q, k, block_table, seq_lens, scale):
     """Every row's scaled logits in row order (b * H_q + h_q), tokens in order: float64."""
-    dt = _dtype_name(shape)
-    q, k = _bits(q, dt), _bits(k, dt)
+    dt, kdt = _dtype_name(shape), _kv_dtype_name(shape)
+    q, k = _bits(q, dt), _bits(k, kdt)
     bt = None if block_table is None else np.ascontiguousarray(block_table, dtype=np.int32)
     sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
     out = np.zeros(int(sl.astype(np.int64).sum()) * shape.num_q_heads, np.float64)
@@ -143,8 +157,8 @@ def logits(shape, q, k, block_table, seq_lens, scale):
 
 def split_partial(shape, q, k, v, block_table, b, h, tokens, scale):
     """Returns (O_s [d], m_s, l_s, L_s) for the given token indices."""
-    dt = _dtype_name(shape)
-    q, k, v = _bits(q, dt), _bits(k, dt), _bits(v, dt)
+    dt, kdt = _dtype_name(shape), _kv_dtype_name(shape)
+    q, k, v = _bits(q, dt), _bits(k, kdt), _bits(v, kdt)
     bt = None if block_table is None else np.ascontiguousarray(block_table, dtype=np.int32)
     tok = np.ascontiguousarray(tokens, dtype=np.int64)
     o = np.zeros(shape.head_dim, np.float64)
@@ -183,8 +197,8 @@ def lse_merge_alpha(o_s, L_s):
 def unified_row(shape, q, k, v, block_table, seq_lens, b, h, scale, phi, range_lo, range_hi,
                 split_tokens=0):
     """Returns (out [d], lse, flag, flagged_partitions) of the unified-max form."""
-    dt = _dtype_name(shape)
-    q, k, v = _bits(q, dt), _bits(k, dt), _bits(v, dt)
+    dt, kdt = _dtype_name(shape), _kv_dtype_name(shape)
+    q, k, v = _bits(q, dt), _bits(k, kdt), _bits(v, kdt)
     bt = None if block_table is None else np.ascontiguousarray(block_table, dtype=np.int32)
     sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
     out = np.zeros(shape.head_dim, np.float64)

@@ -51,6 +51,23 @@ static double decode_bf16(uint16_t h) {
   return (double)f;
 }
 
+/* E4M3 ("E4M3FN"): sign, 4-bit exponent e with bias 7, 3-bit mantissa m. e = 0 is
+ * subnormal, m * 2^-9 (= m/8 * 2^-6); e = 15 with m = 7 is NaN; every other code is
+ * (1 + m/8) * 2^(e - 7), up to 448. There are no infinities. */
+static double decode_e4m3(uint8_t c) {
+  const int sign = (c >> 7) & 1;
+  const int e = (c >> 3) & 0xf;
+  const int m = c & 0x7;
+  double mag;
+  if (e == 0xf && m == 0x7)
+    mag = NAN;
+  else if (e == 0)
+    mag = ldexp((double)m, -9);
+  else
+    mag = ldexp(8.0 + (double)m, e - 10); /* (1 + m/8) * 2^(e-7) */
+  return sign ? -mag : mag;
+}
+
 double oracle_load(int dtype, const void* base, int64_t index) {
   switch (dtype) {
     case ORACLE_F32: {
@@ -68,6 +85,8 @@ double oracle_load(int dtype, const void* base, int64_t index) {
       memcpy(&h, (const char*)base + index * 2, sizeof h);
       return decode_bf16(h);
     }
+    case ORACLE_E4M3:
+      return decode_e4m3(((const uint8_t*)base)[index]);
     default:
       return NAN;
   }
@@ -79,6 +98,8 @@ static int shape_ok(const oracle_shape* s) {
     return 0;
   if (s->num_q_heads % s->num_kv_heads) return 0;
   if (s->dtype < ORACLE_F32 || s->dtype > ORACLE_BF16) return 0;
+  if (s->kv_e4m3 != 0 && s->kv_e4m3 != 1) return 0;
+  if (s->kv_e4m3 && !(isfinite(s->k_scale) && isfinite(s->v_scale))) return 0;
   if (s->paged) {
     if (s->page_size <= 0 || s->max_blocks_per_seq < 0 || s->num_physical_blocks < 0) return 0;
   } else if (s->max_seq_len < 0) {
@@ -121,6 +142,19 @@ int oracle_gather_offsets(const oracle_shape* s, const int32_t* block_table,
   return 0;
 }
 
+/* Element `index` of the K / V cache: in q's encoding, or for an FP8 cache the code's
+ * value times the tensor's scale ([HB] "A paged decode attention kernel (with GQA)": the
+ * cache is "really BF16 or FP8", converted on read). */
+static double load_k(const oracle_shape* s, const void* k, int64_t index) {
+  return s->kv_e4m3 ? oracle_load(ORACLE_E4M3, k, index) * s->k_scale
+                    : oracle_load(s->dtype, k, index);
+}
+
+static double load_v(const oracle_shape* s, const void* v, int64_t index) {
+  return s->kv_e4m3 ? oracle_load(ORACLE_E4M3, v, index) * s->v_scale
+                    : oracle_load(s->dtype, v, index);
+}
+
 /* [HB] "A paged decode attention kernel (with GQA)": several query heads share one KV
  * head, kv_head = head / (num_heads / num_kv_heads). */
 static int kv_head_of(const oracle_shape* s, int h) {
@@ -135,7 +169,7 @@ static double logit(const oracle_shape* s, const void* q, const void* k, int b, 
   const int64_t qoff = ((int64_t)b * s->num_q_heads + h) * d;
   double dot = 0.0;
   for (int64_t i = 0; i < d; ++i)
-    dot += oracle_load(s->dtype, q, qoff + i) * oracle_load(s->dtype, k, koff + i);
+    dot += oracle_load(s->dtype, q, qoff + i) * load_k(s, k, koff + i);
   return scale * dot;
 }
 
@@ -193,7 +227,7 @@ static int one_row(const oracle_shape* s, const void* q, const void* k, const vo
     for (int64_t t = 0; t < n; ++t) l += exp(x[t] - m);
     for (int64_t t = 0; t < n; ++t) {
       const double p = exp(x[t] - m);
-      for (int64_t i = 0; i < d; ++i) out[i] += p * oracle_load(s->dtype, v, off[t] + i);
+      for (int64_t i = 0; i < d; ++i) out[i] += p * load_v(s, v, off[t] + i);
     }
     for (int64_t i = 0; i < d; ++i) out[i] /= l;
     if (lse) *lse = m + log(l);
@@ -271,7 +305,7 @@ int oracle_split_partial(const oracle_shape* s, const void* q, const void* k, co
     for (int64_t j = 0; j < ntok; ++j) l += exp(x[j] - m);
     for (int64_t j = 0; j < ntok; ++j) {
       const double p = exp(x[j] - m);
-      for (int64_t i = 0; i < d; ++i) o_s[i] += p * oracle_load(s->dtype, v, off[j] + i);
+      for (int64_t i = 0; i < d; ++i) o_s[i] += p * load_v(s, v, off[j] + i);
     }
     for (int64_t i = 0; i < d; ++i) o_s[i] /= l;
     *m_s = m;
@@ -382,7 +416,7 @@ int oracle_unified_row(const oracle_shape* s, const void* q, const void* k, cons
       if (outside_distance(x, phi, range_lo, range_hi) > 0.0) flag_j = 1;
       const double f = exp(x - phi);
       den_j += f;
-      for (int64_t i = 0; i < d; ++i) num_j[i] += f * oracle_load(s->dtype, v, off + i);
+      for (int64_t i = 0; i < d; ++i) num_j[i] += f * load_v(s, v, off + i);
     }
     den += den_j;
     for (int64_t i = 0; i < d; ++i) num[i] += num_j[i];

@@ -25,8 +25,10 @@
 extern "C" {
 #endif
 
-/* Element encodings the oracle reads exactly (bit for bit) from storage. */
-enum { ORACLE_F32 = 0, ORACLE_F16 = 1, ORACLE_BF16 = 2 };
+/* Element encodings the oracle reads exactly (bit for bit) from storage. ORACLE_E4M3 is
+ * the 8-bit floating-point format with 4 exponent bits (bias 7) and 3 mantissa bits, no
+ * infinities and S.1111.111 as NaN ("E4M3FN"); it is used only for K and V caches. */
+enum { ORACLE_F32 = 0, ORACLE_F16 = 1, ORACLE_BF16 = 2, ORACLE_E4M3 = 3 };
 
 typedef struct {
   int batch;                /* B */
@@ -40,6 +42,10 @@ typedef struct {
   int max_seq_len;          /* token capacity per sequence (contiguous only) */
   int num_physical_blocks;  /* size of the paged pool (paged only) */
   int dtype;                /* ORACLE_F32 / ORACLE_F16 / ORACLE_BF16 for q, k and v */
+  int kv_e4m3;              /* 1: k and v are ORACLE_E4M3 codes (q stays dtype), each */
+  double k_scale;           /* element standing for code * k_scale / code * v_scale    */
+  double v_scale;           /* ("FlashAttention and inference kernels": an FP8 KV cache, */
+                            /* converted on read); 0: k, v in dtype, scales unused     */
 } oracle_shape;
 
 /* Exact value of element `index` of an array stored in `dtype`. */

@@ -14,8 +14,13 @@ import numpy as np
 
 
 def decode(bits, dtype):
-    """float64 values of fp32 / fp16 / bf16 storage, by NumPy's own conversions."""
+    """float64 values of fp32 / fp16 / bf16 storage, by NumPy's own conversions, and of
+    e4m3 codes by PyTorch's float8_e4m3fn (NumPy has no 8-bit float)."""
     a = np.asarray(bits)
+    if dtype == "e4m3":
+        import torch
+        codes = torch.from_numpy(np.ascontiguousarray(a.astype(np.uint8)))
+        return codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
     if dtype == "f32":
         return a.astype(np.float32).astype(np.float64)
     if dtype == "f16":
@@ -26,13 +31,19 @@ def decode(bits, dtype):
 
 
 def reference(q_bits, k_bits, v_bits, dtype, seq_lens, scale, *, num_kv_heads, paged=False,
-              page_size=16, block_table=None, phi=0.0, range_lo=-math.inf, range_hi=math.inf):
+              page_size=16, block_table=None, phi=0.0, range_lo=-math.inf, range_hi=math.inf,
+              kv_dtype=None, k_scale=1.0, v_scale=1.0):
     """q: [B, Hq, d]; k, v: [B, T, Hkv, d] (contiguous) or [nblocks, page, Hkv, d] (paged).
+    kv_dtype="e4m3": k, v are FP8 codes standing for code * k_scale, code * v_scale.
 
     Returns (out [B, Hq, d], lse [B, Hq], flag [B, Hq])."""
     q = decode(q_bits, dtype)
-    k = decode(k_bits, dtype)
-    v = decode(v_bits, dtype)
+    if kv_dtype == "e4m3":
+        k = decode(k_bits, "e4m3") * k_scale
+        v = decode(v_bits, "e4m3") * v_scale
+    else:
+        k = decode(k_bits, dtype)
+        v = decode(v_bits, dtype)
     B, Hq, d = q.shape
     group = Hq // num_kv_heads
     out = np.zeros((B, Hq, d))

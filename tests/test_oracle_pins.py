@@ -423,3 +423,74 @@ def test_logits_agree_with_the_attention_oracle(paged):
             m = xs.max()
             assert abs(m + math.log(np.exp(xs - m).sum()) - lse[r]) < 1e-12
     assert at == x.size
+
+
+# ---------------------------------------------------------------------------------------
+# FP8 (E4M3) K / V caches ("FlashAttention and inference kernels", "A paged decode
+# attention kernel (with GQA)": the cache is BF16 or FP8, converted on read)
+# ---------------------------------------------------------------------------------------
+def test_e4m3_decoding_matches_library_conversion_and_hand_values():
+    codes = np.arange(256, dtype=np.uint8)
+    got = np.array([oracle.load("e4m3", codes, i) for i in range(256)])
+    lib_vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(lib_vals)
+    assert np.array_equal(np.isnan(got), nan) and list(np.nonzero(nan)[0]) == [0x7F, 0xFF]
+    assert np.array_equal(got[~nan], lib_vals[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(lib_vals[~nan]))
+    # by hand from the format: 1.0, the largest value, the smallest normal and subnormal,
+    # a subnormal with two mantissa bits, negative zero
+    for c, want in [(0x38, 1.0), (0x7E, 448.0), (0x08, 2.0 ** -6), (0x01, 2.0 ** -9),
+                    (0x06, 6 * 2.0 ** -9), (0xB8, -1.0), (0x3D, 1.625)]:
+        assert got[c] == want, (hex(c), got[c], want)
+    assert got[0x80] == 0.0 and np.signbit(got[0x80])
+
+
+def _fp8_codes(rng, shape):
+    """Random E4M3 codes, every one but the two NaNs possible."""
+    mag = rng.integers(0, 0x7F, size=shape)
+    return (mag | (rng.integers(0, 2, size=shape) << 7)).astype(np.uint8)
+
+
+def _tiny_fp8_case(rng, paged, B, Hq, Hkv, d, lens, page, k_scale, v_scale):
+    shape, q, _, _, table, sl = _tiny_case(rng, "bf16", paged, B, Hq, Hkv, d, lens, page, False)
+    if paged:
+        kshape = (shape.num_physical_blocks, page, Hkv, d)
+    else:
+        kshape = (B, shape.max_seq_len, Hkv, d)
+    shape.kv_e4m3, shape.k_scale, shape.v_scale = 1, k_scale, v_scale
+    return shape, q, _fp8_codes(rng, kshape), _fp8_codes(rng, kshape), table, sl
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_brute_force_tiny_fp8_kv(paged):
+    rng = np.random.default_rng(51 + paged)
+    for B, Hq, Hkv, d, page in [(1, 1, 1, 1, 1), (2, 4, 2, 3, 4), (2, 8, 1, 8, 16)]:
+        lens = list(rng.integers(0, 41, size=B))
+        lens[0] = max(lens[0], 1)
+        ks, vs = 0.0137, 0.21
+        shape, q, k, v, table, sl = _tiny_fp8_case(rng, paged, B, Hq, Hkv, d, lens, page, ks, vs)
+        scale = 1.0 / math.sqrt(d)
+        out, lse, flag, _ = oracle.decode_attn(shape, q, k, v, table, sl, scale, 0.5, -2.0, 2.0)
+        ref_o, ref_l, ref_f = oracle_np.reference(q, k, v, "bf16", sl, scale, num_kv_heads=Hkv,
+                                                  paged=paged, page_size=page, block_table=table,
+                                                  phi=0.5, range_lo=-2.0, range_hi=2.0,
+                                                  kv_dtype="e4m3", k_scale=ks, v_scale=vs)
+        np.testing.assert_allclose(out, ref_o.reshape(-1, d), rtol=1e-11, atol=1e-12)
+        finite = np.isfinite(ref_l.ravel())
+        np.testing.assert_allclose(lse[finite], ref_l.ravel()[finite], rtol=1e-12, atol=1e-12)
+        np.testing.assert_array_equal(flag, ref_f.ravel())
+
+
+def test_fp8_scales_act_linearly():
+    """Doubling k_scale is doubling the softmax scale (the logits are scale * k_scale *
+    q . code); doubling v_scale doubles the output and leaves the lse alone. Both by powers
+    of two, so the results agree bit for bit."""
+    rng = np.random.default_rng(53)
+    shape, q, k, v, table, sl = _tiny_fp8_case(rng, True, 2, 4, 2, 16, [37, 20], 8, 0.01, 0.3)
+    base = oracle.decode_attn(shape, q, k, v, table, sl, 0.25)
+    shape.k_scale = 0.02
+    twice_k = oracle.decode_attn(shape, q, k, v, table, sl, 0.125)
+    assert np.array_equal(base[0], twice_k[0]) and np.array_equal(base[1], twice_k[1])
+    shape.k_scale, shape.v_scale = 0.01, 0.6
+    twice_v = oracle.decode_attn(shape, q, k, v, table, sl, 0.25)
+    assert np.array_equal(2.0 * base[0], twice_v[0]) and np.array_equal(base[1], twice_v[1])
