@@ -356,7 +356,7 @@ def run_ours(args):
         "data": "synthetic (seeded N(0,1), workloads.py recipe)",
         "config": {"workload": wl.name, "batch": wl.batch, "q_heads": wl.num_q_heads,
                    "kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
-                   "kv_tokens_per_seq": int(inp.seq_lens.max()), "kv_dtype": wl.dtype,
+                   "kv_tokens_per_seq": int(inp.seq_lens.max()), "kv_dtype": wl.kv_storage,
                    "out_dtype": wl.out_dtype, "softmax": args.mode,
                    "splits": "heuristic (balanced shares)" if args.num_splits < 0 else args.num_splits,
                    "grid_ctas": attn.info.grid_ctas, "stages": attn.info.stages,

@@ -52,6 +52,9 @@ class da_problem(ctypes.Structure):
         ("range_hi", ctypes.c_float),
         ("validate", ctypes.c_int),
         ("num_sms", ctypes.c_int),
+        ("kv_fp8", ctypes.c_int),
+        ("k_scale", ctypes.c_float),
+        ("v_scale", ctypes.c_float),
     ]
 
 
@@ -272,11 +275,17 @@ def decode_attn_destroy(plan):
 def make_problem(*, batch, num_q_heads, num_kv_heads, head_dim, qkv_dtype, out_dtype, paged=False,
                  page_size=16, max_blocks_per_seq=0, num_physical_blocks=0, max_seq_len=0,
                  mode="sync", unified_max=0.0, range_lo=-64.0, range_hi=64.0, validate=False,
-                 num_sms=0) -> da_problem:
+                 num_sms=0, kv_dtype=None, k_scale=1.0, v_scale=1.0) -> da_problem:
+    """kv_dtype=None: K / V stored as qkv_dtype; "e4m3": an FP8 cache of codes standing for
+    code * k_scale and code * v_scale (q stays qkv_dtype, which must be bf16)."""
+    if kv_dtype not in (None, qkv_dtype, "e4m3"):
+        raise ValueError("K / V are stored as qkv_dtype or as e4m3")
+    fp8 = kv_dtype == "e4m3"
     return da_problem(batch, num_q_heads, num_kv_heads, head_dim, int(bool(paged)), page_size,
                       max_blocks_per_seq, num_physical_blocks, max_seq_len,
                       DTYPE_CODES[qkv_dtype], DTYPE_CODES[out_dtype], MODE_CODES[mode],
-                      unified_max, range_lo, range_hi, int(bool(validate)), num_sms)
+                      unified_max, range_lo, range_hi, int(bool(validate)), num_sms, int(fp8),
+                      k_scale if fp8 else 1.0, v_scale if fp8 else 1.0)
 
 
 # ---- torch-facing convenience (marshalling only) -------------------------------------------
@@ -311,9 +320,12 @@ class DecodeAttention:
         import torch
         pr = self.problem
         qkv = self._qkv_dtype
-        for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
-            if t.device.type != "cuda" or t.dtype != qkv or not t.is_contiguous():
-                raise ValueError(f"{name} must be a contiguous CUDA tensor of {qkv}")
+        # an FP8 cache holds E4M3 codes: torch.float8_e4m3fn, or their bytes as uint8
+        kv_ok = (torch.uint8, torch.float8_e4m3fn) if pr.kv_fp8 else (qkv,)
+        for name, t, ok in (("q", q, (qkv,)), ("k_cache", k_cache, kv_ok),
+                            ("v_cache", v_cache, kv_ok)):
+            if t.device.type != "cuda" or t.dtype not in ok or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous CUDA tensor of {ok}")
         if seq_lens.dtype != torch.int32 or seq_lens.device.type != "cuda":
             raise ValueError("seq_lens must be an int32 CUDA tensor")
         if block_table is not None and (block_table.dtype != torch.int32 or

@@ -15,7 +15,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libdecode_attn.so")
-SOURCES = ["da_api.cu", "da_kernels_f32.cu", "da_kernels_f16.cu", "da_kernels_bf16.cu"]
+SOURCES = ["da_api.cu", "da_kernels_f32.cu", "da_kernels_f16.cu", "da_kernels_bf16.cu",
+           "da_kernels_fp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-I" + INCLUDE, "-I" + CSRC]

@@ -21,6 +21,7 @@ namespace da {
 const void* kernel_f32(int head_dim, int group, int mode);
 const void* kernel_f16(int head_dim, int group, int mode);
 const void* kernel_bf16(int head_dim, int group, int mode);
+const void* kernel_fp8(int head_dim, int group, int mode);
 
 // The element offset the kernel reads token t of (b, kvh) from: the same token_row() the
 // producer warp uses for its TMA box coordinates.
@@ -190,6 +191,7 @@ struct da_plan {
   da_problem prob;
   int num_sms;
   int group, es, unit, box_tokens, capacity, n_groups, piece_units;
+  int kv_es;                    // K / V bytes per element (1: FP8 E4M3 cache; else es)
   int policy, num_splits;       // the plan's default split choice
   int grid;                     // balanced grid (or the default uniform grid)
   int recompute_splits, max_splits;
@@ -247,6 +249,14 @@ int validate_problem(const da_problem& p) {
     if (p.max_seq_len < 1) return DA_ERR_INVALID_ARG;
     if ((long long)p.batch * p.max_seq_len >= (1ll << 31)) return DA_ERR_INVALID_ARG;
   }
+  if (p.kv_fp8 != 0 && p.kv_fp8 != 1) return DA_ERR_INVALID_ARG;
+  if (p.kv_fp8) {
+    // FP8 caches run on the tensor-core consumers: bf16 q, groups of 4 or 8 heads
+    if (p.qkv_dtype != DA_BF16 || (G != 4 && G != 8)) return DA_ERR_UNSUPPORTED;
+    if (!std::isfinite(p.k_scale) || !std::isfinite(p.v_scale) || !(p.k_scale > 0.f) ||
+        !(p.v_scale > 0.f))
+      return DA_ERR_INVALID_ARG;
+  }
   if (p.mode != DA_SOFTMAX_SYNC) {
     if (!std::isfinite(p.unified_max) || !std::isfinite(p.range_lo) ||
         !std::isfinite(p.range_hi) || !(p.range_lo < p.range_hi))
@@ -256,6 +266,7 @@ int validate_problem(const da_problem& p) {
 }
 
 const void* kernel_for(const da_plan& pl, int mode) {
+  if (pl.prob.kv_fp8) return kernel_fp8(pl.prob.head_dim, pl.group, mode);
   switch (pl.prob.qkv_dtype) {
     case DA_F32: return kernel_f32(pl.prob.head_dim, pl.group, mode);
     case DA_F16: return kernel_f16(pl.prob.head_dim, pl.group, mode);
@@ -307,8 +318,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // [tokens, Hkv, D] view of a K or V cache; one box = box_tokens rows of one KV head. The
-// tensor-core kernels read the tile with ldmatrix and need the 128-byte swizzle, whose rows
-// are at most 128 bytes: for them the view is 4-D, [tokens, Hkv, D / 64, 64].
+// bf16 tensor-core kernels read the tile with ldmatrix and need the 128-byte swizzle, whose
+// rows are at most 128 bytes: for them the view is 4-D, [tokens, Hkv, D / 64, 64]. FP8 tiles
+// keep the 3-D view (a row of D = 64 or 128 bytes), 128-byte-swizzled when D = 128.
 int make_kv_map(const da_plan& pl, const void* base, bool swizzled, CUtensorMap* map) {
   auto fn = encode_fn();
   if (!fn) {
@@ -319,18 +331,20 @@ int make_kv_map(const da_plan& pl, const void* base, bool swizzled, CUtensorMap*
   const cuuint64_t tokens = p.paged ? (cuuint64_t)p.num_physical_blocks * p.page_size
                                     : (cuuint64_t)p.batch * p.max_seq_len;
   const cuuint64_t dims[3] = {(cuuint64_t)p.head_dim, (cuuint64_t)p.num_kv_heads, tokens};
-  const cuuint64_t strides[2] = {(cuuint64_t)p.head_dim * pl.es,
-                                 (cuuint64_t)p.num_kv_heads * p.head_dim * pl.es};
+  const int es = pl.kv_es;
+  const cuuint64_t strides[2] = {(cuuint64_t)p.head_dim * es,
+                                 (cuuint64_t)p.num_kv_heads * p.head_dim * es};
   const cuuint32_t box[3] = {(cuuint32_t)p.head_dim, 1u, (cuuint32_t)pl.box_tokens};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
-  const CUtensorMapDataType dt =
-      pl.es == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  const CUtensorMapDataType dt = es == 4   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : es == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
+                                           : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   CUresult r;
-  if (swizzled) {
+  if (swizzled && es == 2) {
     const cuuint64_t dims4[4] = {64u, (cuuint64_t)p.head_dim / 64u, (cuuint64_t)p.num_kv_heads,
                                  tokens};
-    const cuuint64_t strides4[3] = {64u * pl.es, (cuuint64_t)p.head_dim * pl.es,
-                                    (cuuint64_t)p.num_kv_heads * p.head_dim * pl.es};
+    const cuuint64_t strides4[3] = {64u * es, (cuuint64_t)p.head_dim * es,
+                                    (cuuint64_t)p.num_kv_heads * p.head_dim * es};
     const cuuint32_t box4[4] = {64u, (cuuint32_t)p.head_dim / 64u, 1u,
                                 (cuuint32_t)pl.box_tokens};
     const cuuint32_t estr4[4] = {1u, 1u, 1u, 1u};
@@ -338,8 +352,9 @@ int make_kv_map(const da_plan& pl, const void* base, bool swizzled, CUtensorMap*
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else {
+    const bool swz8 = swizzled && es == 1 && p.head_dim == 128;
     r = fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, swz8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   }
   if (r != CUDA_SUCCESS) {
@@ -381,6 +396,7 @@ void fill_common(const da_plan& pl, Params& k, const int32_t* block_table,
   k.piece_units = pl.piece_units;
   k.box_tokens = pl.box_tokens;
   k.out_dtype = p.out_dtype;
+  k.v_scale = 1.f;
   k.n_groups = pl.n_groups;
   k.stages = pl.stages;
   k.batch_smem = pl.batch_smem;
@@ -440,12 +456,13 @@ int decode_attn_plan(const da_problem* problem, int num_splits, da_plan** plan_o
   pl->num_sms = sms;
   pl->group = p.num_q_heads / p.num_kv_heads;
   pl->es = elem_size(p.qkv_dtype);
+  pl->kv_es = p.kv_fp8 ? 1 : pl->es;
   pl->unit = p.paged ? std::max(16, p.page_size) : 16;
   pl->box_tokens = p.paged ? std::min(p.page_size, kStageTokens) : kStageTokens;
   pl->capacity = p.paged ? p.max_blocks_per_seq * p.page_size : p.max_seq_len;
   pl->n_groups = p.batch * p.num_kv_heads;
   {
-    const long long unit_bytes = 2LL * pl->unit * p.head_dim * pl->es;   // K + V of one unit
+    const long long unit_bytes = 2LL * pl->unit * p.head_dim * pl->kv_es;   // K + V of one unit
     pl->piece_units = (int)((kPieceCostBytes + unit_bytes / 2) / unit_bytes);
   }
   const long long units_max = (pl->capacity + pl->unit - 1) / pl->unit;
@@ -485,7 +502,7 @@ int decode_attn_plan(const da_problem* problem, int num_splits, da_plan** plan_o
   // deepest pipeline that fits the per-CTA shared memory limit
   pl->stages = 0;
   for (int s = kMaxStages; s >= 2; --s) {
-    const Layout L = make_layout(p.head_dim, pl->group, pl->es, s, pl->batch_smem);
+    const Layout L = make_layout(p.head_dim, pl->group, pl->es, s, pl->batch_smem, pl->kv_es);
     if (L.total <= kSmemLimit) {
       pl->stages = s;
       pl->smem_bytes = L.total;
@@ -614,7 +631,7 @@ int decode_attn_run_ex(const da_plan* plan, const da_run_args* args) {
   const bool unified = p.mode == DA_SOFTMAX_UNIFIED;   // the recompute launch follows
 
   // tensor-core kernels (both modes, so the recompute pass too) read 128-byte-swizzled tiles
-  const bool mma = uses_mma(pl.es, p.qkv_dtype == DA_BF16, pl.group);
+  const bool mma = uses_mma(pl.kv_es, p.qkv_dtype == DA_BF16, pl.group);
   CUtensorMap tmk, tmv;
   int rc = make_kv_map(pl, k_cache, mma, &tmk);
   if (rc == DA_OK) rc = make_kv_map(pl, v_cache, mma, &tmv);
@@ -630,7 +647,8 @@ int decode_attn_run_ex(const da_plan* plan, const da_run_args* args) {
   kp.num_splits = S;
   kp.list_flags = unified ? 1 : 0;
   const double log2e = 1.4426950408889634;
-  kp.qscale = (float)((double)scale * log2e);
+  kp.qscale = (float)((double)scale * log2e * (p.kv_fp8 ? (double)p.k_scale : 1.0));
+  kp.v_scale = p.kv_fp8 ? p.v_scale : 1.f;
   kp.phi2 = (float)((double)p.unified_max * log2e);
   kp.lo2 = (float)(((double)p.unified_max + p.range_lo) * log2e);
   kp.hi2 = (float)(((double)p.unified_max + p.range_hi) * log2e);
@@ -748,6 +766,7 @@ int decode_attn_logit_histogram(const da_plan* plan, const void* q, const void* 
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(seq_lens, 4) ||
       !aligned(counts, 8) || (block_table && !aligned(block_table, 4)))
     return DA_ERR_INVALID_ARG;
+  if (pl.prob.kv_fp8) return DA_ERR_UNSUPPORTED;
   if (nbins < 1 || nbins > DECODE_ATTN_MAX_HIST_BINS) return DA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !std::isfinite(lo) || !std::isfinite(hi) || !(lo < hi))
     return DA_ERR_INVALID_ARG;

@@ -45,6 +45,20 @@ enum Policy { kBalanced = 0, kUniform = 1 };
 enum SoftmaxMode { kSoftmaxSync = 0, kSoftmaxUnified = 1, kSoftmaxUnifiedLocal = 2 };
 enum OutType { kOutF32 = 0, kOutF16 = 1, kOutBF16 = 2 };
 
+// FP8 storage of K and V: one E4M3 code per element (sign, 4-bit exponent with bias 7, 3-bit
+// mantissa; no infinities), standing for code * k_scale or code * v_scale. q stays bf16.
+struct fp8e4m3 {
+  uint8_t bits;
+};
+template <typename T>
+struct QOf {   // q's storage type for a K / V storage type
+  using type = T;
+};
+template <>
+struct QOf<fp8e4m3> {
+  using type = __nv_bfloat16;
+};
+
 struct Params {
   const void* q;                 // [B, Hq, D]
   const int32_t* block_table;    // [B, max_blocks] (paged)
@@ -76,7 +90,8 @@ struct Params {
   int n_groups;                  // B * Hkv
   int stages;                    // pipeline depth
   int batch_smem;                // lengths held in smem (balanced) or 0
-  float qscale;                  // scale * log2(e): logits come out in log2 units
+  float qscale;                  // scale * log2(e) (* k_scale): logits in log2 units
+  float v_scale;                 // FP8 V: the outputs' factor (1 otherwise)
   float phi2, lo2, hi2;          // unified constant and range bounds, log2 units
 };
 
@@ -89,11 +104,13 @@ struct Layout {
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-// Split kernels whose consumers run on the tensor cores (see da_mma.cuh), in either softmax
-// mode: bf16 caches, packed groups of 4 or 8 query heads. Their K/V tiles are TMA-loaded with
-// the 128-byte swizzle (4-D view: 64-element rows, d / 64 of them per token, heads, tokens).
+// Split kernels whose consumers run on the tensor cores (see da_mma.cuh), in every softmax
+// mode: bf16 or FP8 caches (es: K / V bytes per element), packed groups of 4 or 8 query
+// heads. bf16 tiles are TMA-loaded with the 128-byte swizzle (4-D view: 64-element rows,
+// d / 64 of them per token, heads, tokens); FP8 tiles as rows of d bytes (3-D view), with the
+// 128-byte swizzle when d = 128.
 __host__ __device__ constexpr bool uses_mma(int es, bool is_bf16, int G) {
-  return es == 2 && is_bf16 && (G == 4 || G == 8);
+  return (es == 1 || (es == 2 && is_bf16)) && (G == 4 || G == 8);
 }
 
 // Geometry of a consumer warp's logit transpose: a KV row of D elements of es bytes is split
@@ -119,9 +136,11 @@ __host__ __device__ constexpr int warp_scratch_floats(int D, int G, int es) {
   return (m + 3) / 4 * 4;
 }
 
-__host__ __device__ inline Layout make_layout(int D, int G, int es, int stages, int batch_smem) {
+// es: q's bytes per element (also the consumer scratch geometry's); kv_es: K / V's (0: es).
+__host__ __device__ inline Layout make_layout(int D, int G, int es, int stages, int batch_smem,
+                                              int kv_es = 0) {
   Layout L;
-  const uint32_t kv = (uint32_t)kStageTokens * D * es;
+  const uint32_t kv = (uint32_t)kStageTokens * D * (kv_es ? kv_es : es);
   L.k_off = 0;
   L.v_off = kv;
   L.q_off = 2 * kv;

@@ -45,7 +45,10 @@ namespace da {
 
 template <typename T, int D, int G>
 struct Cfg {
-  static constexpr int kEs = sizeof(T);
+  using Q = typename QOf<T>::type;                    // q's storage (bf16 over FP8 K / V)
+  static constexpr bool kFp8 = std::is_same<T, fp8e4m3>::value;
+  static constexpr int kEs = sizeof(T);                 // K / V bytes per element
+  static constexpr int kQEs = sizeof(Q);
   static constexpr int kEpl = 16 / kEs;               // elements per 16-byte chunk
   static constexpr int kLg = D / kEpl;                // lanes per KV row (lane group)
   static constexpr int kNlg = 32 / kLg;               // lane groups per warp
@@ -54,7 +57,7 @@ struct Cfg {
   static constexpr int kNv = kV >= kLg ? kV / kLg : 1;    // complete logits per lane
   static constexpr int kRep = kV >= kLg ? 1 : kLg / kV;   // lanes that hold the same logit
   static constexpr int kRowBytes = D * kEs;
-  static constexpr int kQBytes = G * D * kEs;
+  static constexpr int kQBytes = G * D * kQEs;
   static_assert(kLg >= 1 && kLg <= 32 && (32 % kLg) == 0, "a row must span a lane group");
   static_assert((kTokensPerWarp % kNlg) == 0, "rows per warp must split over lane groups");
   static_assert((kV & (kV - 1)) == 0, "logit count must be a power of two");
@@ -166,7 +169,7 @@ __device__ __forceinline__ void run_producer(const Params& p, Sched s, uint8_t* 
     if (pc.t1 <= pc.t0) continue;
     const int32_t* trow = p.paged ? p.block_table + (long long)pc.b * p.max_blocks : nullptr;
     const char* qsrc = static_cast<const char*>(p.q) +
-                       ((long long)pc.b * p.hq + (long long)pc.kvh * G) * D * C::kEs;
+                       ((long long)pc.b * p.hq + (long long)pc.kvh * G) * D * C::kQEs;
     // Block-table entries of pages [wbase, wbase + 32) (win) and [wbase + 32, wbase + 64)
     // (wnext), one per lane; wnext is loaded a window ahead of its first use.
     int wbase = -(1 << 30);
@@ -549,7 +552,7 @@ template <typename T, int D, int G>
 __device__ __forceinline__ void publish_mma(const MmaState<D, G>& st, float m0, float m1,
                                             uint32_t fmask, float* mm, float* ml,
                                             uint32_t* mflag, float* wbuf, int warp, int lane) {
-  constexpr int W = warp_scratch_floats(D, G, (int)sizeof(T));
+  constexpr int W = warp_scratch_floats(D, G, Cfg<T, D, G>::kQEs);
   const int hp = 2 * (lane & 3), dr = lane >> 2;
   float den0 = st.den[0], den1 = st.den[1];
 #pragma unroll
@@ -558,16 +561,19 @@ __device__ __forceinline__ void publish_mma(const MmaState<D, G>& st, float m0, 
     den1 += __shfl_xor_sync(0xffffffffu, den1, o);
   }
   const uint32_t fm = __reduce_or_sync(0xffffffffu, fmask);
-  float* w0 = wbuf + warp * W + hp * D + dr;
+  float* w0 = wbuf + warp * W + hp * D;
 #pragma unroll
   for (int mt = 0; mt < D / 16; ++mt) {
+    // the O^T rows this lane holds: d and d + 8 (bf16 tiles), d and d + 1 (FP8 tiles)
+    const int d = Cfg<T, D, G>::kFp8 ? (D / 8) * dr + 2 * mt : mt * 16 + dr;
+    const int d2 = Cfg<T, D, G>::kFp8 ? d + 1 : d + 8;
     if (hp < G) {
-      w0[mt * 16] = st.o[mt][0];
-      w0[mt * 16 + 8] = st.o[mt][2];
+      w0[d] = st.o[mt][0];
+      w0[d2] = st.o[mt][2];
     }
     if (hp + 1 < G) {
-      w0[D + mt * 16] = st.o[mt][1];
-      w0[D + mt * 16 + 8] = st.o[mt][3];
+      w0[D + d] = st.o[mt][1];
+      w0[D + d2] = st.o[mt][3];
     }
   }
   if (lane < 4) {
@@ -595,7 +601,7 @@ __device__ __forceinline__ void combine_piece(const Params& p, const Piece& pc, 
                                               int ctid) {
   constexpr int kCT = kConsumerWarps * 32;
   constexpr float kLn2 = 0.6931471805599453f;
-  constexpr int W = warp_scratch_floats(D, G, (int)sizeof(T));
+  constexpr int W = warp_scratch_floats(D, G, Cfg<T, D, G>::kQEs);
   named_bar_sync(1, kCT);
 
   uint32_t fl = 0;
@@ -624,7 +630,7 @@ __device__ __forceinline__ void combine_piece(const Params& p, const Piece& pc, 
     const float o = sum > 0.f ? num / sum : 0.f;
     const float L2 = sum > 0.f ? M + fast_log2(sum) : -INFINITY;
     if (direct) {
-      store_out(p.out, (row0 + g) * D + d, p.out_dtype, o);
+      store_out(p.out, (row0 + g) * D + d, p.out_dtype, o * p.v_scale);
       if (d == 0) {
         if (p.out_lse) p.out_lse[row0 + g] = L2 * kLn2;
         if (p.row_flags && first_phase) p.row_flags[row0 + g] = (uint8_t)((fl >> g) & 1u);
@@ -740,7 +746,8 @@ __device__ __forceinline__ void combine_piece(const Params& p, const Piece& pc, 
         const int d0 = e0 - g * D;
 #pragma unroll
         for (int i = 0; i < EPT; ++i)
-          store_out(p.out, (row0 + g) * D + d0 + i, p.out_dtype, sum > 0.f ? num[i] / sum : 0.f);
+          store_out(p.out, (row0 + g) * D + d0 + i, p.out_dtype,
+                    sum > 0.f ? num[i] / sum * p.v_scale : 0.f);
         if (d0 == 0) {
           if (p.out_lse)
             p.out_lse[row0 + g] = sum > 0.f ? (hmax[g] + fast_log2(sum)) * kLn2 : -INFINITY;
@@ -862,7 +869,8 @@ __device__ __forceinline__ void run_consumers_mma(const Params& p, Sched s, uint
   int* misc = reinterpret_cast<int*>(smem + L.misc_off);
   const int ctid = warp * 32 + lane;
   const int row0 = warp * kTokensPerWarp;
-  const MmaLane<D> mlane(row0, lane);
+  constexpr bool kFp8 = Cfg<T, D, G>::kFp8;
+  const std::conditional_t<kFp8, NoMmaLane, MmaLane<D>> mlane(row0, lane);
   Piece pc;
   while (sched_next(s, p, pc)) {
     MmaState<D, G> st;
@@ -874,6 +882,7 @@ __device__ __forceinline__ void run_consumers_mma(const Params& p, Sched s, uint
     st.m[0] = st.m[1] = -INFINITY;
     st.mt[0] = st.mt[1] = -INFINITY;
     st.sw = false;
+    st.qmul = p.qscale;   // FP8 tiles: reset with q's scale when q is loaded
     uint32_t fmask = 0;
     const int nst = (pc.t1 - pc.t0 + kStageTokens - 1) / kStageTokens;
     for (int j = 0; j < nst; j += 2) {
@@ -889,14 +898,24 @@ __device__ __forceinline__ void run_consumers_mma(const Params& p, Sched s, uint
       }
       const uint8_t* st0 = stages + s0 * L.stage_bytes;
       const uint8_t* st1 = stages + s1 * L.stage_bytes;
-      if (j == 0) mma_load_q<D, G>(st, st0 + L.q_off, lane);
+      if (j == 0) {
+        if constexpr (kFp8)
+          mma_load_q_fp8<D, G>(p, st, st0 + L.q_off, lane);
+        else
+          mma_load_q<D, G>(st, st0 + L.q_off, lane);
+      }
       const int ts = pc.t0 + j * kStageTokens;
       const int n[2] = {min(kStageTokens, pc.t1 - ts),
                         pair ? min(kStageTokens, pc.t1 - ts - kStageTokens) : 0};
       const uint8_t* const st1m = pair ? st1 : st0;   // no second stage: read stage 0 again
       const uint32_t kt[2] = {smem_u32(st0 + L.k_off), smem_u32(st1m + L.k_off)};
       const uint32_t vt[2] = {smem_u32(st0 + L.v_off), smem_u32(st1m + L.v_off)};
-      if (!dead) mma_consume<D, G, UNIFIED, LOCAL>(p, st, mlane, kt, vt, n, row0, lane, fmask);
+      if (!dead) {
+        if constexpr (kFp8)
+          mma_consume_fp8<D, G, UNIFIED, LOCAL>(p, st, kt, vt, n, row0, lane, fmask);
+        else
+          mma_consume<D, G, UNIFIED, LOCAL>(p, st, mlane, kt, vt, n, row0, lane, fmask);
+      }
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&empty[s0]);
@@ -960,7 +979,7 @@ __device__ __forceinline__ void consumer_role(const Params& p, int warp, int lan
   using C = Cfg<T, D, G>;
   constexpr bool kMma = uses_mma(sizeof(T), std::is_same<T, __nv_bfloat16>::value, G);
   uint8_t* smem = smem_base();
-  const Layout L = make_layout(D, G, C::kEs, p.stages, p.batch_smem);
+  const Layout L = make_layout(D, G, C::kQEs, p.stages, p.batch_smem, C::kEs);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   uint64_t* empty = full + p.stages;
   const Sched s = launch_sched(p, reinterpret_cast<const int*>(smem + L.lens_off),
@@ -983,9 +1002,10 @@ __device__ __forceinline__ void producer_role(const Params& p, const CUtensorMap
                                               const CUtensorMap* tmv, int warp, int lane) {
   using C = Cfg<T, D, G>;
   constexpr bool kMma = uses_mma(sizeof(T), std::is_same<T, __nv_bfloat16>::value, G);
+  constexpr bool k4d = kMma && !C::kFp8;   // bf16 tensor-core tiles: the 4-D swizzled view
   if (warp >= kConsumerWarps + (p.paged ? 4 : 2)) return;
   uint8_t* smem = smem_base();
-  const Layout L = make_layout(D, G, C::kEs, p.stages, p.batch_smem);
+  const Layout L = make_layout(D, G, C::kQEs, p.stages, p.batch_smem, C::kEs);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   uint64_t* empty = full + p.stages;
   const Sched s = launch_sched(p, reinterpret_cast<const int*>(smem + L.lens_off),
@@ -993,7 +1013,7 @@ __device__ __forceinline__ void producer_role(const Params& p, const CUtensorMap
                                reinterpret_cast<const int*>(smem + L.misc_off));
   uint32_t k = 0;
   bool dead = false;
-  run_producer<T, D, G, kMma>(p, s, smem, L, full, empty, tmk, tmv, lane, warp - kConsumerWarps,
+  run_producer<T, D, G, k4d>(p, s, smem, L, full, empty, tmk, tmv, lane, warp - kConsumerWarps,
                               k, dead);
 }
 
@@ -1018,7 +1038,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   {
     uint8_t* smem = smem_base();
-    const Layout L = make_layout(D, G, C::kEs, p.stages, p.batch_smem);
+    const Layout L = make_layout(D, G, C::kQEs, p.stages, p.batch_smem, C::kEs);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
     uint64_t* empty = full + p.stages;
     int* lens = reinterpret_cast<int*>(smem + L.lens_off);
@@ -1120,6 +1140,19 @@ inline const void* pick_kernel(int G, int mode) {
       return nullptr;
   }
 #undef DA_CASE
+}
+
+// FP8 caches run on the tensor-core consumers only: groups of 4 or 8 heads.
+template <typename T, int D>
+inline const void* pick_kernel_mma(int G, int mode) {
+  if (G != 4 && G != 8) return nullptr;
+  if (G == 4)
+    return mode == kSoftmaxSync      ? (const void*)&decode_split_kernel<T, D, 4, 0>
+           : mode == kSoftmaxUnified ? (const void*)&decode_split_kernel<T, D, 4, 1>
+                                     : (const void*)&decode_split_kernel<T, D, 4, 2>;
+  return mode == kSoftmaxSync      ? (const void*)&decode_split_kernel<T, D, 8, 0>
+         : mode == kSoftmaxUnified ? (const void*)&decode_split_kernel<T, D, 8, 1>
+                                   : (const void*)&decode_split_kernel<T, D, 8, 2>;
 }
 
 }  // namespace da

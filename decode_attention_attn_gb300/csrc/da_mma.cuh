@@ -1,5 +1,5 @@
 // da_mma.cuh -- tensor-core consumer for packed GQA groups of G >= 4 query heads over bf16
-// caches, in both softmax modes.
+// or FP8 (E4M3) caches, in every softmax mode (FP8 tiles: f16 MMAs, see the end of the file).
 //
 // Per KV tile the group's work is two dense contractions (the logits of G heads against the
 // tile's tokens, and P . V). On CUDA cores they made the split kernel issue-bound on GB300
@@ -48,6 +48,16 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// D += A (16x16) * B (16x8), f16 inputs, FP32 accumulators.
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // Transpose of an 8x8 matrix of 16-bit values held in the warp's fragment layout.
 __device__ __forceinline__ uint32_t movm_t(uint32_t x) {
   uint32_t r;
@@ -55,11 +65,68 @@ __device__ __forceinline__ uint32_t movm_t(uint32_t x) {
   return r;
 }
 
+// Two FP32 values -> f16x2 (round to nearest even); `hi_elem` lands in the upper half.
+__device__ __forceinline__ uint32_t f16x2_rn(float lo_elem, float hi_elem) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi_elem), "f"(lo_elem));
+  return r;
+}
+__device__ __forceinline__ float f16_lo(uint32_t h) {
+  return __half2float(__ushort_as_half((unsigned short)(h & 0xffffu)));
+}
+__device__ __forceinline__ float f16_hi(uint32_t h) {
+  return __half2float(__ushort_as_half((unsigned short)(h >> 16)));
+}
+
 // Two FP32 values -> bf16x2 (round to nearest even); `hi_elem` lands in the upper half.
 __device__ __forceinline__ uint32_t bf16x2_rn(float lo_elem, float hi_elem) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi_elem), "f"(lo_elem));
   return r;
+}
+
+// ---- FP8 (E4M3) tiles ----------------------------------------------------------------------
+// Two E4M3 codes (the low 16 bits of c; the lower code lands in the lower half) -> f16x2.
+// Every E4M3 value is a normal binary16 number or zero, so the conversion is exact. (A NaN
+// code converts to a NaN; caches hold none.)
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t c) {
+  uint32_t h;
+  asm("{\n\t.reg .b16 lo;\n\tcvt.u16.u32 lo, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+      : "=r"(h)
+      : "r"(c));
+  return h;
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+// Bytes of {b, a} picked by the selector's nibbles (byte i of the result = byte s_i).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+// Byte offset of 16-byte chunk c of token row t in an FP8 tile of 64 rows of D bytes, as the
+// TMA box writes it: with the 128-byte swizzle for D = 128 (chunk c of row t at chunk
+// c ^ (t mod 8)), unswizzled for D = 64.
+template <int D>
+__device__ __forceinline__ uint32_t fp8_off(int t, int c) {
+  if constexpr (D == 128)
+    return (uint32_t)(t * 128 + ((c ^ (t & 7)) << 4));
+  else
+    return (uint32_t)(t * D + c * 16);
 }
 
 // Byte offset of element e (a multiple of 8) of row t in a tile written by a TMA box of
@@ -91,16 +158,24 @@ struct MmaLane {
   }
 };
 
+// FP8 tiles need no ldmatrix addresses.
+struct NoMmaLane {
+  __device__ __forceinline__ NoMmaLane(int, int) {}
+};
+
 template <int D, int G>
 struct MmaState {
   static constexpr int KS = D / 16;     // k-steps of the logits / m-tiles of the output
   uint32_t qb[KS][2];                   // B fragments of q^T (k = d, n = head); heads >= G zero
-  float o[KS][4];                       // O^T: [0] (d, head hp), [1] (d, hp + 1), [2] (d + 8, hp),
-                                        // [3] (d + 8, hp + 1) with d = 16 mt + lane / 4
+  float o[KS][4];                       // O^T: [0] (d, head hp), [1] (d, hp + 1), [2] (d', hp),
+                                        // [3] (d', hp + 1) with d = 16 mt + lane / 4, d' = d + 8
+                                        // (FP8 tiles: d = (D/8)(lane / 4) + 2 mt, d' = d + 1)
   float den[2];                         // this lane's share of heads hp, hp + 1 denominators
   float m[2];                           // synchronised recurrence: their running maxima
   float mt[2];                          // split-local fallback, before the switch: the lane's
                                         // maximum logit of each head so far
+  float qmul;                           // logit factor: scale * log2 e (FP8 tiles: times 2^-s,
+                                        // s the power of two q was scaled by)
   bool sw;                              // split-local fallback: the warp has switched to the
                                         // synchronised recurrence
 };
@@ -118,30 +193,21 @@ __device__ __forceinline__ void mma_load_q(MmaState<D, G>& st, const uint8_t* qs
   }
 }
 
-// Consume the warp's 8 rows of two consecutive stages (16 tokens = one MMA k-extent of P . V).
-// kt / vt: shared-memory addresses of the K and V tiles of stages 0 and 1 (with n[1] == 0 there
-// is no second stage: the caller passes stage 0's tiles again and every stage-1 token is
-// masked, so no stale shared memory enters the MMA).
-template <int D, int G, bool UNIFIED, bool LOCAL>
-__device__ __forceinline__ void mma_consume(const Params& p, MmaState<D, G>& st,
-                                            const MmaLane<D>& ml, const uint32_t (&kt)[2],
-                                            const uint32_t (&vt)[2], const int (&n)[2], int row0,
-                                            int lane, uint32_t& fmask) {
+// One stage pair's softmax step, shared by the bf16 and FP8 consumers: the logits from the
+// two S^T accumulator chains sa, sb (token lane/4 of stage 0 in [0], [1], of stage 1 in
+// [2], [3]; heads hp, hp + 1), the range check, the running maxima of the synchronised
+// recurrence, p, the denominators, and P^T as hi / lo B fragments (bh*, bl*): bf16, or f16
+// when F16. f16 holds only p <= 2^15 and loses p below 2^-24, so in the unified phase (p
+// relative to phi, of any size) the F16 step takes each head's p relative to the stage pair's
+// own maximum m_t and returns f = 2^(m_t - phi) per head (f0, f1): the caller adds the pair's
+// P . V to the accumulators times f, which is the same sum. f0 = f1 = 1 otherwise.
+template <int D, int G, bool UNIFIED, bool LOCAL, bool F16>
+__device__ __forceinline__ void mma_softmax(const Params& p, MmaState<D, G>& st,
+                                            const float (&sa)[4], const float (&sb)[4],
+                                            const int (&n)[2], int row0, int lane,
+                                            uint32_t& fmask, uint32_t& bh0, uint32_t& bh1,
+                                            uint32_t& bl0, uint32_t& bl1, float& f0, float& f1) {
   constexpr int KS = MmaState<D, G>::KS;
-  const uint32_t kbase = ml.kst ? kt[1] : kt[0], vbase = ml.vst ? vt[1] : vt[0];
-
-  // S^T = K q^T: two accumulator chains (even and odd k-steps) halve the dependent latency
-  float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int kk = 0; kk < KS; ++kk) {
-    uint32_t a0, a1, a2, a3;
-    ldsm_x4(kbase + ml.koff[kk], a0, a1, a2, a3);
-    if (kk & 1)
-      mma_bf16(sb, a0, a1, a2, a3, st.qb[kk][0], st.qb[kk][1]);
-    else
-      mma_bf16(sa, a0, a1, a2, a3, st.qb[kk][0], st.qb[kk][1]);
-  }
-
   // The lane's logits: [0], [1] = token lane/4 of stage 0 for heads hp, hp + 1; [2], [3] = the
   // same row of stage 1. A head's 16 logits sit in the 8 lanes that share lane % 4.
   const int hp = 2 * (lane & 3), tr = row0 + (lane >> 2);
@@ -149,7 +215,7 @@ __device__ __forceinline__ void mma_consume(const Params& p, MmaState<D, G>& st,
   bool valid[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    x[c] = (sa[c] + sb[c]) * p.qscale;
+    x[c] = (sa[c] + sb[c]) * st.qmul;
     valid[c] = hp + (c & 1) < G && tr < n[c >> 1];
   }
   float ref0 = p.phi2, ref1 = p.phi2;
@@ -217,33 +283,92 @@ __device__ __forceinline__ void mma_consume(const Params& p, MmaState<D, G>& st,
     }
     ref0 = st.m[0];   // -inf only while all of the head's tokens so far are masked
     ref1 = st.m[1];
+  } else if constexpr (F16) {
+    // unified phase, f16 P: each head's p relative to its maximum over this stage pair
+    float m0 = fmaxf(valid[0] ? x[0] : -INFINITY, valid[2] ? x[2] : -INFINITY);
+    float m1 = fmaxf(valid[1] ? x[1] : -INFINITY, valid[3] ? x[3] : -INFINITY);
+#pragma unroll
+    for (int o = 4; o <= 16; o <<= 1) {
+      m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+    }
+    ref0 = m0 > -INFINITY ? m0 : p.phi2;
+    ref1 = m1 > -INFINITY ? m1 : p.phi2;
+    f0 = m0 > -INFINITY ? fast_exp2(m0 - p.phi2) : 0.f;
+    f1 = m1 > -INFINITY ? fast_exp2(m1 - p.phi2) : 0.f;
   }
   float pr[4];
+  if (!F16 || !UNIFIED || (LOCAL && st.sw)) f0 = f1 = 1.f;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     pr[c] = valid[c] ? fast_exp2(x[c] - ((c & 1) ? ref1 : ref0)) : 0.f;
     if (UNIFIED && valid[c] && (x[c] < p.lo2 || x[c] > p.hi2)) fmask |= 1u << (hp + (c & 1));
   }
-  st.den[0] += pr[0] + pr[2];
-  st.den[1] += pr[1] + pr[3];
+  st.den[0] += f0 * (pr[0] + pr[2]);
+  st.den[1] += f1 * (pr[1] + pr[3]);
 
-  // P as bf16 hi + lo (lower half = head hp), transposed into B fragments of P^T:
+  // P as hi + lo (lower half = head hp), transposed into B fragments of P^T:
   // b0 = stage-0 tokens 2 (lane % 4), +1 of head lane / 4, b1 = the same of stage 1
-  const uint32_t h0 = bf16x2_rn(pr[0], pr[1]), h1 = bf16x2_rn(pr[2], pr[3]);
-  const uint32_t l0 = bf16x2_rn(pr[0] - __uint_as_float(h0 << 16),
-                                pr[1] - __uint_as_float(h0 & 0xffff0000u));
-  const uint32_t l1 = bf16x2_rn(pr[2] - __uint_as_float(h1 << 16),
-                                pr[3] - __uint_as_float(h1 & 0xffff0000u));
-  const uint32_t bh0 = movm_t(h0), bh1 = movm_t(h1), bl0 = movm_t(l0), bl1 = movm_t(l1);
+  uint32_t h0, h1, l0, l1;
+  if constexpr (F16) {
+    h0 = f16x2_rn(pr[0], pr[1]);
+    h1 = f16x2_rn(pr[2], pr[3]);
+    l0 = f16x2_rn(pr[0] - f16_lo(h0), pr[1] - f16_hi(h0));
+    l1 = f16x2_rn(pr[2] - f16_lo(h1), pr[3] - f16_hi(h1));
+  } else {
+    h0 = bf16x2_rn(pr[0], pr[1]);
+    h1 = bf16x2_rn(pr[2], pr[3]);
+    l0 = bf16x2_rn(pr[0] - __uint_as_float(h0 << 16), pr[1] - __uint_as_float(h0 & 0xffff0000u));
+    l1 = bf16x2_rn(pr[2] - __uint_as_float(h1 << 16), pr[3] - __uint_as_float(h1 & 0xffff0000u));
+  }
+  bh0 = movm_t(h0);
+  bh1 = movm_t(h1);
+  bl0 = movm_t(l0);
+  bl1 = movm_t(l1);
 
-  // V rows of masked tokens are zeroed in the fragments (0 * NaN would poison the MMA); only
-  // a warp whose rows run past a stage's end needs it
-  uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+}
+
+// Masks that zero the V fragments' halves of tokens past a stage's end (0 * NaN would poison
+// the MMA): vm0 for stage 0, vm1 for stage 1; all ones for a warp whose rows are all valid.
+__device__ __forceinline__ void v_masks(const int (&n)[2], int row0, int lane, uint32_t& vm0,
+                                        uint32_t& vm1) {
+  vm0 = 0xffffffffu;
+  vm1 = 0xffffffffu;
   if (!(row0 + kTokensPerWarp <= n[0] && row0 + kTokensPerWarp <= n[1])) {
     const int tk = row0 + 2 * (lane & 3);
     vm0 = (tk < n[0] ? 0x0000ffffu : 0u) | (tk + 1 < n[0] ? 0xffff0000u : 0u);
     vm1 = (tk < n[1] ? 0x0000ffffu : 0u) | (tk + 1 < n[1] ? 0xffff0000u : 0u);
   }
+}
+
+// Consume the warp's 8 rows of two consecutive stages (16 tokens = one MMA k-extent of P . V).
+// kt / vt: shared-memory addresses of the K and V tiles of stages 0 and 1 (with n[1] == 0 there
+// is no second stage: the caller passes stage 0's tiles again and every stage-1 token is
+// masked, so no stale shared memory enters the MMA).
+template <int D, int G, bool UNIFIED, bool LOCAL>
+__device__ __forceinline__ void mma_consume(const Params& p, MmaState<D, G>& st,
+                                            const MmaLane<D>& ml, const uint32_t (&kt)[2],
+                                            const uint32_t (&vt)[2], const int (&n)[2], int row0,
+                                            int lane, uint32_t& fmask) {
+  constexpr int KS = MmaState<D, G>::KS;
+  const uint32_t kbase = ml.kst ? kt[1] : kt[0], vbase = ml.vst ? vt[1] : vt[0];
+
+  // S^T = K q^T: two accumulator chains (even and odd k-steps) halve the dependent latency
+  float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int kk = 0; kk < KS; ++kk) {
+    uint32_t a0, a1, a2, a3;
+    ldsm_x4(kbase + ml.koff[kk], a0, a1, a2, a3);
+    if (kk & 1)
+      mma_bf16(sb, a0, a1, a2, a3, st.qb[kk][0], st.qb[kk][1]);
+    else
+      mma_bf16(sa, a0, a1, a2, a3, st.qb[kk][0], st.qb[kk][1]);
+  }
+  uint32_t bh0, bh1, bl0, bl1, vm0, vm1;
+  float f0, f1;
+  mma_softmax<D, G, UNIFIED, LOCAL, false>(p, st, sa, sb, n, row0, lane, fmask, bh0, bh1, bl0,
+                                           bl1, f0, f1);
+  v_masks(n, row0, lane, vm0, vm1);
 
   // O^T += V^T P^T: per m-tile of 16 d, A fragments (d 0-7 | 8-15) x (stage-0 | stage-1 tokens)
 #pragma unroll
@@ -256,6 +381,156 @@ __device__ __forceinline__ void mma_consume(const Params& p, MmaState<D, G>& st,
     a3 &= vm1;
     mma_bf16(st.o[mt], a0, a1, a2, a3, bh0, bh1);
     mma_bf16(st.o[mt], a0, a1, a2, a3, bl0, bl1);
+  }
+}
+
+// ---- FP8 caches ------------------------------------------------------------------------
+// The same two contractions over E4M3 tiles, on f16 MMAs: every E4M3 code is a binary16
+// number, converted exactly by one cvt per pair of codes. ldmatrix cannot transpose byte
+// tiles, so each lane reads its operand bytes with plain shared-memory loads, and both
+// contractions use an order of their index sets that makes a lane's bytes contiguous:
+//   S^T = K q^T sums over d, in any order as long as K and q^T agree: k-step kk takes, in the
+//   fragment slots of lane (g, c) = (lane / 4, lane % 4), d = c * D/4 + 4 kk + {0, 1} (slots
+//   2c, 2c + 1) and + {2, 3} (slots 2c + 8, 2c + 9). The lane's K bytes for all k-steps are
+//   then D/4 consecutive bytes of its row, and q^T is loaded in the same order. q (bf16) is
+//   scaled by a power of two 2^s into f16's range, exactly for every element above 2^-29
+//   of the group's largest (f16 has 11 significant bits to bf16's 8), and the logits are
+//   scaled back by 2^-s.
+//   O^T += V^T P^T keeps the token order (P^T's B fragment comes out of the S^T layout) and
+//   permutes the output rows instead: row r of m-tile mt is d = (D/8) * (r mod 8) + 2 mt +
+//   r / 8, so lane (g, c) holds d = (D/8) g + 2 mt + {0, 1} of tokens 2c, 2c + 1 of each
+//   stage, D/8 consecutive bytes of each of four rows for all m-tiles; prmt pairs the two
+//   tokens' bytes of one d. publish_mma undoes the row order. P enters as f16 hi + lo (see
+//   mma_softmax for its range).
+
+// q^T fragments in the FP8 order (see above) from the stage's q area (G x D bf16), as f16
+// scaled by 2^s with s such that the group's largest |q| lands in [2^14, 2^15); st.qmul
+// becomes qscale * 2^-s.
+template <int D, int G>
+__device__ __forceinline__ void mma_load_q_fp8(const Params& p, MmaState<D, G>& st,
+                                               const uint8_t* qsm, int lane) {
+  constexpr int KS = MmaState<D, G>::KS;
+  const int head = lane >> 2, c = lane & 3;
+  const bool hv = head < G;
+  uint32_t raw[KS][2];
+  float amax = 0.f;
+#pragma unroll
+  for (int k = 0; k < KS; ++k) {
+    const __nv_bfloat16* qr =
+        reinterpret_cast<const __nv_bfloat16*>(qsm) + head * D + c * (D / 4) + 4 * k;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      raw[k][i] = hv ? *reinterpret_cast<const uint32_t*>(qr + 2 * i) : 0u;
+      amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(raw[k][i] << 16)),
+                               fabsf(__uint_as_float(raw[k][i] & 0xffff0000u))));
+    }
+  }
+#pragma unroll
+  for (int o = 1; o <= 16; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  // amax = 0.f1 * 2^e with e = biased exponent - 126; s = 15 - e, kept where 2^s and 2^-s
+  // are normal floats
+  const int e = (int)((__float_as_uint(amax) >> 23) & 0xffu) - 126;
+  const int sh = amax > 0.f ? min(126, max(-126, 15 - e)) : 0;
+  const float up = __uint_as_float((uint32_t)(127 + sh) << 23);
+  const float down = __uint_as_float((uint32_t)(127 - sh) << 23);
+#pragma unroll
+  for (int k = 0; k < KS; ++k)
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+      st.qb[k][i] = f16x2_rn(__uint_as_float(raw[k][i] << 16) * up,
+                             __uint_as_float(raw[k][i] & 0xffff0000u) * up);
+  st.qmul = p.qscale * down;
+}
+
+// mma_consume over FP8 tiles (kt / vt, n, row0 as there).
+template <int D, int G, bool UNIFIED, bool LOCAL>
+__device__ __forceinline__ void mma_consume_fp8(const Params& p, MmaState<D, G>& st,
+                                                const uint32_t (&kt)[2], const uint32_t (&vt)[2],
+                                                const int (&n)[2], int row0, int lane,
+                                                uint32_t& fmask) {
+  constexpr int KS = MmaState<D, G>::KS;
+  constexpr int KW = D / 16;   // 4-byte words of a lane's K bytes (one per k-step)
+  const int g = lane >> 2, c = lane & 3;
+
+  // S^T = K q^T: A rows 0-7 = token row0 + g of stage 0, rows 8-15 = the same of stage 1
+  uint32_t k0[KW], k1[KW];
+  {
+    const int t = row0 + g;
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h) {   // 16-byte chunks c * D/64 + h of the row
+      const uint4 w0 = lds128(kt[0] + fp8_off<D>(t, c * (D / 64) + h));
+      const uint4 w1 = lds128(kt[1] + fp8_off<D>(t, c * (D / 64) + h));
+      k0[4 * h] = w0.x; k0[4 * h + 1] = w0.y; k0[4 * h + 2] = w0.z; k0[4 * h + 3] = w0.w;
+      k1[4 * h] = w1.x; k1[4 * h + 1] = w1.y; k1[4 * h + 2] = w1.z; k1[4 * h + 3] = w1.w;
+    }
+  }
+  float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int kk = 0; kk < KS; ++kk) {
+    const uint32_t a0 = e4m3x2_to_f16x2(k0[kk]), a2 = e4m3x2_to_f16x2(k0[kk] >> 16);
+    const uint32_t a1 = e4m3x2_to_f16x2(k1[kk]), a3 = e4m3x2_to_f16x2(k1[kk] >> 16);
+    if (kk & 1)
+      mma_f16(sb, a0, a1, a2, a3, st.qb[kk][0], st.qb[kk][1]);
+    else
+      mma_f16(sa, a0, a1, a2, a3, st.qb[kk][0], st.qb[kk][1]);
+  }
+  uint32_t bh0, bh1, bl0, bl1, vm0, vm1;
+  float f0, f1;
+  mma_softmax<D, G, UNIFIED, LOCAL, true>(p, st, sa, sb, n, row0, lane, fmask, bh0, bh1, bl0,
+                                          bl1, f0, f1);
+  const bool scaled = UNIFIED && !(LOCAL && st.sw);   // the unified phase: P . V times f
+  v_masks(n, row0, lane, vm0, vm1);
+  const bool tail = (vm0 & vm1) != 0xffffffffu;
+
+  // O^T += V^T P^T: the lane's D/8 bytes (d = (D/8) g + 0 .. D/8 - 1) of tokens row0 + 2c and
+  // row0 + 2c + 1 of both stages; word w of a row covers m-tiles 2w and 2w + 1
+  constexpr int VW = D / 32;   // 4-byte words per row and lane
+  uint32_t va[VW], vb[VW], vc[VW], vd[VW];
+  {
+    const int t = row0 + 2 * c;
+    if constexpr (D == 128) {
+      const uint4 x = lds128(vt[0] + fp8_off<D>(t, g)), y = lds128(vt[0] + fp8_off<D>(t + 1, g));
+      const uint4 z = lds128(vt[1] + fp8_off<D>(t, g)), u = lds128(vt[1] + fp8_off<D>(t + 1, g));
+      va[0] = x.x; va[1] = x.y; va[2] = x.z; va[3] = x.w;
+      vb[0] = y.x; vb[1] = y.y; vb[2] = y.z; vb[3] = y.w;
+      vc[0] = z.x; vc[1] = z.y; vc[2] = z.z; vc[3] = z.w;
+      vd[0] = u.x; vd[1] = u.y; vd[2] = u.z; vd[3] = u.w;
+    } else {
+      const uint32_t o = (uint32_t)(8 * g);
+      const uint2 x = lds64(vt[0] + t * D + o), y = lds64(vt[0] + (t + 1) * D + o);
+      const uint2 z = lds64(vt[1] + t * D + o), u = lds64(vt[1] + (t + 1) * D + o);
+      va[0] = x.x; va[1] = x.y;
+      vb[0] = y.x; vb[1] = y.y;
+      vc[0] = z.x; vc[1] = z.y;
+      vd[0] = u.x; vd[1] = u.y;
+    }
+  }
+#pragma unroll
+  for (int mt = 0; mt < KS; ++mt) {
+    // bytes [token 2c, token 2c + 1] of d (the lower half) and of d + 1 (the upper half)
+    const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+    const uint32_t x0 = prmt(va[mt >> 1], vb[mt >> 1], sel);
+    const uint32_t x1 = prmt(vc[mt >> 1], vd[mt >> 1], sel);
+    uint32_t a0 = e4m3x2_to_f16x2(x0), a1 = e4m3x2_to_f16x2(x0 >> 16);
+    uint32_t a2 = e4m3x2_to_f16x2(x1), a3 = e4m3x2_to_f16x2(x1 >> 16);
+    if (tail) {
+      a0 &= vm0;
+      a1 &= vm0;
+      a2 &= vm1;
+      a3 &= vm1;
+    }
+    if (scaled) {
+      float t4[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_f16(t4, a0, a1, a2, a3, bh0, bh1);
+      mma_f16(t4, a0, a1, a2, a3, bl0, bl1);
+      st.o[mt][0] = fmaf(f0, t4[0], st.o[mt][0]);
+      st.o[mt][1] = fmaf(f1, t4[1], st.o[mt][1]);
+      st.o[mt][2] = fmaf(f0, t4[2], st.o[mt][2]);
+      st.o[mt][3] = fmaf(f1, t4[3], st.o[mt][3]);
+    } else {
+      mma_f16(st.o[mt], a0, a1, a2, a3, bh0, bh1);
+      mma_f16(st.o[mt], a0, a1, a2, a3, bl0, bl1);
+    }
   }
 }
 

@@ -13,6 +13,11 @@ round-to-nearest-even cast to the storage dtype):
 
 The five named workloads have the shapes of the pages' models: Llama2-7B-shaped MHA
 (32 heads of 128), a GQA model with 32 query heads over 8 KV heads, and a tiny case.
+
+FP8 caches (kv_dtype "e4m3"): K and V are drawn as above in fp32, then each tensor is
+quantised with one scale, max |x| / 448 (448 is the largest E4M3 value), to E4M3 codes by
+PyTorch's float8_e4m3fn cast (round to nearest even); the cache holds the code bytes and the
+scales (as fp32 numbers) travel with the inputs. q stays bf16.
 """
 from __future__ import annotations
 
@@ -26,7 +31,8 @@ import torch
 SEED_Q, SEED_K, SEED_V, SEED_LENS, SEED_OUTLIERS, SEED_PERM = 1, 2, 3, 4, 5, 7
 
 TORCH_DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
-ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2}
+ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1}
+E4M3_MAX = 448.0
 
 
 @dataclasses.dataclass(frozen=True)
@@ -51,10 +57,15 @@ class Workload:
     outlier_scale: float = 40.0
     lens: Optional[tuple] = None    # explicit per-sequence lengths (overrides the above)
     max_seq_len: int = 0            # contiguous capacity per sequence (0: max length)
+    kv_dtype: Optional[str] = None  # None: K / V stored as dtype; "e4m3": an FP8 cache
 
     @property
     def group(self) -> int:
         return self.num_q_heads // self.num_kv_heads
+
+    @property
+    def kv_storage(self) -> str:
+        return self.kv_dtype or self.dtype
 
     @property
     def scale(self) -> float:
@@ -76,9 +87,15 @@ PAGED_B64 = Workload("paged_b64_h32kv8_d128_n512to8192_bf16", 64, 32, 8, 128, "b
 STRESS_128K = Workload("unified_stress_b1_h32kv8_d128_n131072_bf16", 1, 32, 8, 128, "bf16",
                        "bf16", seq_len=131072, mode="unified", outlier_frac=0.005)
 
-WORKLOADS = {w.name: w for w in (TINY, MHA_4K, GQA_32K, PAGED_B64, STRESS_128K)}
+# The 32K GQA and paged workloads over FP8 (E4M3) caches: the same draws, quantised.
+GQA_32K_FP8 = GQA_32K.replace(name="gqa_b1_h32kv8_d128_n32768_e4m3", kv_dtype="e4m3")
+PAGED_B64_FP8 = PAGED_B64.replace(name="paged_b64_h32kv8_d128_n512to8192_e4m3", kv_dtype="e4m3")
+
+WORKLOADS = {w.name: w for w in (TINY, MHA_4K, GQA_32K, PAGED_B64, STRESS_128K, GQA_32K_FP8,
+                                 PAGED_B64_FP8)}
 ALIASES = {"tiny": TINY.name, "mha": MHA_4K.name, "gqa32k": GQA_32K.name,
-           "paged": PAGED_B64.name, "stress": STRESS_128K.name}
+           "paged": PAGED_B64.name, "stress": STRESS_128K.name,
+           "gqa32k_fp8": GQA_32K_FP8.name, "paged_fp8": PAGED_B64_FP8.name}
 
 
 def get(name: str) -> Workload:
@@ -97,12 +114,14 @@ class Inputs:
     max_blocks_per_seq: int         # paged table width (0 when contiguous)
     num_physical_blocks: int
     outlier_rows: int = 0
+    k_scale: float = 1.0            # FP8 caches: the value of code 1 (an fp32 number)
+    v_scale: float = 1.0
 
     def kv_bytes(self) -> int:
         """Algorithmic K+V bytes of one step: sum_b N_b * H_kv * 2 * d * sizeof."""
         w = self.wl
         return int(self.seq_lens.to(torch.int64).sum()) * w.num_kv_heads * 2 * w.head_dim * \
-            ELEM_BYTES[w.dtype]
+            ELEM_BYTES[w.kv_storage]
 
 
 def _gen(seed: int, offset: int) -> torch.Generator:
@@ -158,6 +177,13 @@ def generate(wl: Workload, offset: int = 0) -> Inputs:
         pick = torch.randperm(Hkv * n_tok, generator=_gen(SEED_OUTLIERS, offset))[:n_out]
         tok, head = pick // Hkv, pick % Hkv
         k32[0, tok, head, :] *= wl.outlier_scale
+    if wl.kv_dtype == "e4m3":
+        k, k_scale = quantize_e4m3(k32)
+        del k32
+        v, v_scale = quantize_e4m3(torch.randn(kv_shape, generator=_gen(SEED_V, offset),
+                                               dtype=torch.float32))
+        return Inputs(wl, q, k, v, block_table, torch.tensor(lens, dtype=torch.int32), cap,
+                      max_blocks, nblocks, n_out, k_scale, v_scale)
     k = k32.to(TORCH_DTYPES[wl.dtype])
     del k32
     v = _normal(kv_shape, SEED_V, offset, wl.dtype)
@@ -165,9 +191,20 @@ def generate(wl: Workload, offset: int = 0) -> Inputs:
                   max_blocks, nblocks, n_out)
 
 
+def quantize_e4m3(x: torch.Tensor):
+    """(E4M3 code bytes as uint8, scale): one fp32 scale for the tensor, max |x| / 448."""
+    amax = float(x.abs().max()) if x.numel() else 0.0
+    scale = float(np.float32(amax / E4M3_MAX)) if amax > 0 else 1.0
+    codes = (x / scale).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes, scale
+
+
 def bits(t: torch.Tensor) -> np.ndarray:
-    """The tensor's storage as numpy: float32 for fp32, uint16 bit patterns for fp16/bf16."""
+    """The tensor's storage as numpy: float32 for fp32, uint16 bit patterns for fp16/bf16,
+    the code bytes (uint8) of an FP8 cache."""
     t = t.contiguous()
     if t.dtype == torch.float32:
         return t.numpy()
+    if t.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return t.view(torch.uint8).numpy()
     return t.view(torch.int16).numpy().view(np.uint16)

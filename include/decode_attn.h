@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define DECODE_ATTN_ABI_VERSION 1
+#define DECODE_ATTN_ABI_VERSION 2
 
 /* Largest bin count decode_attn_logit_histogram accepts. */
 #define DECODE_ATTN_MAX_HIST_BINS 32768
@@ -98,7 +98,7 @@ typedef struct {
   int num_physical_blocks;  /* paged: pool size; num_physical_blocks * page_size < 2^31 */
   int max_seq_len;          /* contiguous: token capacity per sequence;
                                batch * max_seq_len < 2^31 */
-  da_dtype qkv_dtype;       /* storage of q, k_cache and v_cache */
+  da_dtype qkv_dtype;       /* storage of q, k_cache and v_cache (q only when kv_fp8) */
   da_dtype out_dtype;       /* storage of out (rounded to nearest even from fp32) */
   da_softmax_mode mode;
   float unified_max;        /* phi (natural-log units of the scaled logits); UNIFIED modes */
@@ -107,6 +107,18 @@ typedef struct {
   int validate;             /* 1: every run synchronises and reports device findings */
   int num_sms;              /* 0: plan for the current device's SM count; > 0: plan for
                                that many SMs without touching CUDA (host-side planning) */
+  /* FP8 KV cache ("FlashAttention and inference kernels", "A paged decode attention kernel
+   * (with GQA)": the cache is BF16 or FP8, converted to FP32 in registers on read).
+   * kv_fp8 = 1: k_cache and v_cache hold one-byte E4M3 codes (sign, 4-bit exponent with
+   * bias 7, 3-bit mantissa, no infinities, S.1111.111 = NaN; "E4M3FN"), element for element
+   * in the layout above, and code c stands for c * k_scale (K) or c * v_scale (V), scales
+   * finite and > 0; q stays qkv_dtype, which must be DA_BF16, and G must be 4 or 8 (else
+   * DA_ERR_UNSUPPORTED). The codes convert exactly; k_scale enters the logits' FP32 scale
+   * factor and v_scale the output's. NaN codes are not detected (they read as finite
+   * values). kv_fp8 = 0: k_cache and v_cache are qkv_dtype; the scales are not read. */
+  int kv_fp8;
+  float k_scale;
+  float v_scale;
 } da_problem;
 
 typedef struct da_plan da_plan;   /* opaque, host-owned, immutable after creation */
@@ -157,8 +169,8 @@ int decode_attn_workspace_init(const da_plan* plan, void* workspace, size_t work
 
 /* Run one decode step.
  *   q           device, [batch, H_q, d] in qkv_dtype, 16-byte aligned.
- *   k_cache,    device, layout per problem->paged (see da_problem), qkv_dtype, 16-byte
- *   v_cache     aligned.
+ *   k_cache,    device, layout per problem->paged (see da_problem), qkv_dtype (E4M3 codes
+ *   v_cache     when kv_fp8), 16-byte aligned.
  *   block_table device int32 [batch, max_blocks_per_seq] when paged (entries for the
  *               pages a sequence uses must lie in [0, num_physical_blocks); the rest are
  *               ignored, -1 by convention); must be NULL when contiguous.
@@ -288,8 +300,8 @@ int decode_attn_debug_gather(const da_plan* plan, const int32_t* block_table,
  * A token whose block-table entry lies outside the pool, and tokens past the capacity, are
  * not counted: the counts then sum to less than H_q * sum_b min(seq_lens[b], capacity), which
  * the caller can check. Enqueued on `stream`; not synchronised.
- * Errors: INVALID_ARG (null or misaligned pointer, bad range or bin count), UNSUPPORTED,
- * CUDA. */
+ * Errors: INVALID_ARG (null or misaligned pointer, bad range or bin count), UNSUPPORTED (also
+ * for an FP8 cache, which this pass does not read), CUDA. */
 int decode_attn_logit_histogram(const da_plan* plan, const void* q, const void* k_cache,
                                 const int32_t* block_table, const int32_t* seq_lens,
                                 float scale, float lo, float hi, int nbins,

@@ -30,7 +30,8 @@ def oracle_shape(inp: workloads.Inputs):
                              paged=w.paged, page_size=w.page_size,
                              max_blocks_per_seq=inp.max_blocks_per_seq,
                              max_seq_len=inp.max_seq_len,
-                             num_physical_blocks=inp.num_physical_blocks)
+                             num_physical_blocks=inp.num_physical_blocks, kv_dtype=w.kv_dtype,
+                             k_scale=inp.k_scale, v_scale=inp.v_scale)
 
 
 def run_oracle(inp: workloads.Inputs, rows=None, nthreads=None, phi=None, lo=None, hi=None):
@@ -54,7 +55,8 @@ def problem_for(inp: workloads.Inputs, mode=None, out_dtype=None, validate=False
         num_physical_blocks=inp.num_physical_blocks, max_seq_len=inp.max_seq_len,
         mode=mode or w.mode, unified_max=w.phi if phi is None else phi,
         range_lo=w.range_lo if lo is None else lo, range_hi=w.range_hi if hi is None else hi,
-        validate=validate, num_sms=num_sms)
+        validate=validate, num_sms=num_sms, kv_dtype=w.kv_dtype, k_scale=inp.k_scale,
+        v_scale=inp.v_scale)
 
 
 class DeviceInputs:

@@ -34,7 +34,7 @@ def test_library_exports_every_header_symbol(L):
 
 
 def test_abi_version_and_strerror(L):
-    assert binding.decode_attn_abi_version() == 1
+    assert binding.decode_attn_abi_version() == 2
     for code in binding.ERRORS:
         assert binding.decode_attn_strerror(code)
     assert "unknown" in binding.decode_attn_strerror(-99)
@@ -56,11 +56,55 @@ def test_abi_version_and_strerror(L):
     (dict(mode="unified", unified_max=math.inf), -1),
     (dict(mode="unified_local", range_lo=1.0, range_hi=-1.0), -1),
     (dict(num_sms=-1), -1),
+    # FP8 caches: bf16 q, groups of 4 or 8, finite positive scales
+    (dict(kv_dtype="e4m3", k_scale=0.0), -1),
+    (dict(kv_dtype="e4m3", v_scale=-1.0), -1),
+    (dict(kv_dtype="e4m3", k_scale=math.inf), -1),
+    (dict(kv_dtype="e4m3", v_scale=math.nan), -1),
+    (dict(kv_dtype="e4m3", qkv_dtype="f16", out_dtype="f16"), -2),
+    (dict(kv_dtype="e4m3", num_q_heads=16, num_kv_heads=8), -2),   # G = 2
+    (dict(kv_dtype="e4m3", num_q_heads=8, num_kv_heads=8), -2),    # G = 1
 ])
 def test_plan_rejects_bad_problems(L, kw, code):
     with pytest.raises(binding.DecodeAttnError) as e:
         binding.decode_attn_plan(_prob(**kw), 0)
     assert e.value.code == code
+
+
+def test_plan_rejects_a_bad_fp8_flag(L):
+    prob = _prob()
+    prob.kv_fp8 = 2
+    with pytest.raises(binding.DecodeAttnError) as e:
+        binding.decode_attn_plan(prob, 0)
+    assert e.value.code == -1
+
+
+def test_fp8_plan_halves_the_stage_and_the_piece_cost(L):
+    """An FP8 cache moves one byte per K / V element: the stages hold the same 64 tokens in
+    less shared memory (so the pipeline is at least as deep), and a piece's fixed cost is
+    charged in twice as many 16-token units."""
+    plan16, _ = binding.decode_attn_plan(_prob(), 0)
+    plan8, _ = binding.decode_attn_plan(_prob(kv_dtype="e4m3", k_scale=0.01, v_scale=0.02), 0)
+    try:
+        i16, i8 = binding.decode_attn_plan_info(plan16), binding.decode_attn_plan_info(plan8)
+        assert i8.stage_tokens == i16.stage_tokens == 64
+        assert i8.stages >= i16.stages and i8.smem_bytes <= 232448
+        assert i8.grid_ctas == i16.grid_ctas == 152
+    finally:
+        binding.decode_attn_destroy(plan16)
+        binding.decode_attn_destroy(plan8)
+
+
+def test_histogram_refuses_an_fp8_plan(L):
+    plan, _ = binding.decode_attn_plan(_prob(kv_dtype="e4m3", k_scale=0.01, v_scale=0.02), 0)
+    try:
+        fake = 1 << 20   # aligned non-null addresses: the storage check comes first
+        rc = L.decode_attn_logit_histogram(plan, fake, fake, None, fake, ctypes.c_float(0.1),
+                                           ctypes.c_float(-1.0), ctypes.c_float(1.0), 8, fake,
+                                           None)
+        assert rc == -2
+    finally:
+        binding.decode_attn_destroy(plan)
 
 
 def test_plan_rejects_an_unknown_softmax_mode(L):
