@@ -336,6 +336,14 @@ int make_kv_map(const da_plan& pl, const void* base, bool swizzled, CUtensorMap*
                                  (cuuint64_t)p.num_kv_heads * p.head_dim * es};
   const cuuint32_t box[3] = {(cuuint32_t)p.head_dim, 1u, (cuuint32_t)pl.box_tokens};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
+  // L2 fills no wider than a KV row: with a wider promotion every box row also pulls in the
+  // neighbouring head's row, which a paged gather seldom reads before it is evicted (FP8 rows
+  // of 128 bytes under 256-byte promotion: 1.48x the algorithmic DRAM bytes on the paged
+  // batch)
+  const long long row_bytes = (long long)p.head_dim * es;
+  const CUtensorMapL2promotion l2p = row_bytes >= 256   ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                     : row_bytes >= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                                        : CU_TENSOR_MAP_L2_PROMOTION_L2_64B;
   const CUtensorMapDataType dt = es == 4   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                  : es == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
                                            : CU_TENSOR_MAP_DATA_TYPE_UINT8;
@@ -350,12 +358,12 @@ int make_kv_map(const da_plan& pl, const void* base, bool swizzled, CUtensorMap*
     const cuuint32_t estr4[4] = {1u, 1u, 1u, 1u};
     r = fn(map, dt, 4, const_cast<void*>(base), dims4, strides4, box4, estr4,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+           l2p, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else {
     const bool swz8 = swizzled && es == 1 && p.head_dim == 128;
     r = fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
            CU_TENSOR_MAP_INTERLEAVE_NONE, swz8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+           l2p, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   }
   if (r != CUDA_SUCCESS) {
     g_cuda_error = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string((int)r);
