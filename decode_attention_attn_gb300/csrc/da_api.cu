@@ -64,6 +64,39 @@ __device__ __forceinline__ int hist_bin(float x, float lo, float inv_w, int nbin
   return f >= (float)nbins ? nbins + 1 : 1 + (int)f;
 }
 
+// How a lane reads its share of a K row: 16-byte chunks of q's own storage type, or for an
+// FP8 cache 8-byte chunks of E4M3 codes (so that a lane's q, bf16, stays 8 elements) with q
+// read as bf16.
+template <typename T>
+struct HistIO {
+  using Q = T;
+  using KChunk = uint4;
+  static constexpr int kEpc = Elem<T>::kPerChunk;
+  __device__ __forceinline__ static void k_pairs(const uint4& c, f32x2* f) {
+    Elem<T>::to_pairs(c, f);
+  }
+};
+template <>
+struct HistIO<fp8e4m3> {
+  using Q = __nv_bfloat16;
+  using KChunk = uint2;
+  static constexpr int kEpc = 8;
+  __device__ __forceinline__ static void k_pairs(const uint2& c, f32x2* f) {
+    const uint32_t w[2] = {c.x, c.y};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t v = e4m3x2_to_f16x2(h ? w[i] >> 16 : w[i]);
+        __half2 hv;
+        memcpy(&hv, &v, 4);
+        const float2 x = __half22float2(hv);
+        f[2 * i + h] = f2_pack(x.x, x.y);
+      }
+    }
+  }
+};
+
 // One warp per work item (64 tokens of one sequence and KV head); a K row is split over C
 // lanes, 16 bytes each, so a warp reads R = 32 / C rows per load and U loads per lane are in
 // flight before any arithmetic. The pass is latency-bound per warp, so the number of resident
@@ -80,7 +113,10 @@ __global__ void __launch_bounds__(kHistThreads, G == 8 ? (sizeof(T) == 4 ? 3 : 2
                            float scale, float lo, float inv_w, int nbins,
                            unsigned long long* __restrict__ counts) {
   extern __shared__ unsigned hist[];   // [nbins + 2]
-  constexpr int EPC = Elem<T>::kPerChunk;   // elements per 16-byte chunk
+  using IO = HistIO<T>;
+  using Q = typename IO::Q;
+  using KChunk = typename IO::KChunk;
+  constexpr int EPC = IO::kEpc;             // K elements per lane chunk (16 or 8 bytes)
   constexpr int NP = EPC / 2;               // fp32 pairs per chunk
   constexpr int C = D / EPC;                // lanes per K row: 8, 16 or 32
   constexpr int R = 32 / C;                 // K rows per warp load
@@ -108,13 +144,13 @@ __global__ void __launch_bounds__(kHistThreads, G == 8 ? (sizeof(T) == 4 ? 3 : 2
     const int t1 = min(n, t0 + kHistItemTokens);
 
     f32x2 qp[G][NP];
-    const T* qg = static_cast<const T*>(p.q) + ((long long)b * p.hq + (long long)kvh * G) * D;
+    const Q* qg = static_cast<const Q*>(p.q) + ((long long)b * p.hq + (long long)kvh * G) * D;
 #pragma unroll
-    for (int g = 0; g < G; ++g)
-      Elem<T>::to_pairs(__ldg(reinterpret_cast<const uint4*>(qg + g * D) + c), qp[g]);
+    for (int g = 0; g < G; ++g)   // q's chunk c: EPC elements of Q, 16 bytes
+      Elem<Q>::to_pairs(__ldg(reinterpret_cast<const uint4*>(qg + g * D) + c), qp[g]);
 
     for (int tb = t0; tb < t1; tb += R * U) {
-      uint4 kr[U];
+      KChunk kr[U];
       bool ok[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -126,14 +162,14 @@ __global__ void __launch_bounds__(kHistThreads, G == 8 ? (sizeof(T) == 4 ? 3 : 2
           z = token_row(p, b, t, entry);
         }
         ok[u] = z >= 0;
-        kr[u] = make_uint4(0, 0, 0, 0);
+        kr[u] = KChunk{};
         if (ok[u])
-          kr[u] = __ldg(reinterpret_cast<const uint4*>(kc + ((long long)z * p.hkv + kvh) * D) + c);
+          kr[u] = __ldg(reinterpret_cast<const KChunk*>(kc + ((long long)z * p.hkv + kvh) * D) + c);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         f32x2 kf[NP];
-        Elem<T>::to_pairs(kr[u], kf);
+        IO::k_pairs(kr[u], kf);
         float v[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
@@ -774,7 +810,6 @@ int decode_attn_logit_histogram(const da_plan* plan, const void* q, const void* 
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(seq_lens, 4) ||
       !aligned(counts, 8) || (block_table && !aligned(block_table, 4)))
     return DA_ERR_INVALID_ARG;
-  if (pl.prob.kv_fp8) return DA_ERR_UNSUPPORTED;
   if (nbins < 1 || nbins > DECODE_ATTN_MAX_HIST_BINS) return DA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !std::isfinite(lo) || !std::isfinite(hi) || !(lo < hi))
     return DA_ERR_INVALID_ARG;
@@ -782,7 +817,8 @@ int decode_attn_logit_histogram(const da_plan* plan, const void* q, const void* 
   if (!std::isfinite(inv_w) || !(inv_w > 0.f)) return DA_ERR_INVALID_ARG;
 
   const void* fn = nullptr;
-  switch (pl.prob.qkv_dtype) {
+  if (pl.prob.kv_fp8) fn = histogram_kernel_for<fp8e4m3>(pl.prob.head_dim, pl.group);
+  else switch (pl.prob.qkv_dtype) {
     case DA_F32: fn = histogram_kernel_for<float>(pl.prob.head_dim, pl.group); break;
     case DA_F16: fn = histogram_kernel_for<__half>(pl.prob.head_dim, pl.group); break;
     default: fn = histogram_kernel_for<__nv_bfloat16>(pl.prob.head_dim, pl.group); break;
@@ -804,7 +840,9 @@ int decode_attn_logit_histogram(const da_plan* plan, const void* q, const void* 
   Params kp;
   fill_common(pl, kp, block_table, seq_lens, nullptr);
   kp.q = q;
-  void* args[7] = {&kp, &k_cache, &scale, &lo, const_cast<float*>(&inv_w), &nbins, &counts};
+  // an FP8 cache's codes stand for code * k_scale: fold it into the logit scale
+  float xscale = pl.prob.kv_fp8 ? (float)((double)scale * (double)pl.prob.k_scale) : scale;
+  void* args[7] = {&kp, &k_cache, &xscale, &lo, const_cast<float*>(&inv_w), &nbins, &counts};
   e = cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(kHistThreads), args, smem,
                        static_cast<cudaStream_t>(cuda_stream));
   return e == cudaSuccess ? DA_OK : cuda_fail(e, "launching the logit histogram kernel");

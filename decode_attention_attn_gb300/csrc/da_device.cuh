@@ -327,6 +327,17 @@ __device__ __forceinline__ f32x2 f2_mul(f32x2 a, f32x2 b) {
   return r;
 }
 
+// Two E4M3 codes (the low 16 bits of c; the lower code lands in the lower half) -> f16x2.
+// Every E4M3 value is a normal binary16 number or zero, so the conversion is exact. (A NaN
+// code converts to a NaN; caches hold none.)
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t c) {
+  uint32_t h;
+  asm("{\n\t.reg .b16 lo;\n\tcvt.u16.u32 lo, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+      : "=r"(h)
+      : "r"(c));
+  return h;
+}
+
 // ---- element conversion of one 16-byte chunk to FP32 ------------------------------------
 template <typename T>
 struct Elem;

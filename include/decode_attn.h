@@ -300,8 +300,9 @@ int decode_attn_debug_gather(const da_plan* plan, const int32_t* block_table,
  * A token whose block-table entry lies outside the pool, and tokens past the capacity, are
  * not counted: the counts then sum to less than H_q * sum_b min(seq_lens[b], capacity), which
  * the caller can check. Enqueued on `stream`; not synchronised.
- * Errors: INVALID_ARG (null or misaligned pointer, bad range or bin count), UNSUPPORTED (also
- * for an FP8 cache, which this pass does not read), CUDA. */
+ * For an FP8 cache (kv_fp8) the logits are scale * q . (code * k_scale), as decode_attn_run
+ * forms them. Errors: INVALID_ARG (null or misaligned pointer, bad range or bin count),
+ * UNSUPPORTED, CUDA. */
 int decode_attn_logit_histogram(const da_plan* plan, const void* q, const void* k_cache,
                                 const int32_t* block_table, const int32_t* seq_lens,
                                 float scale, float lo, float hi, int nbins,

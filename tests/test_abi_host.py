@@ -95,18 +95,6 @@ def test_fp8_plan_halves_the_stage_and_the_piece_cost(L):
         binding.decode_attn_destroy(plan8)
 
 
-def test_histogram_refuses_an_fp8_plan(L):
-    plan, _ = binding.decode_attn_plan(_prob(kv_dtype="e4m3", k_scale=0.01, v_scale=0.02), 0)
-    try:
-        fake = 1 << 20   # aligned non-null addresses: the storage check comes first
-        rc = L.decode_attn_logit_histogram(plan, fake, fake, None, fake, ctypes.c_float(0.1),
-                                           ctypes.c_float(-1.0), ctypes.c_float(1.0), 8, fake,
-                                           None)
-        assert rc == -2
-    finally:
-        binding.decode_attn_destroy(plan)
-
-
 def test_plan_rejects_an_unknown_softmax_mode(L):
     prob = _prob()
     prob.mode = 3

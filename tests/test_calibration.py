@@ -120,6 +120,10 @@ CALIB_CASES = [
     W.Workload("calib_g2_d64_f16", 3, 4, 2, 64, "f16", "f16", lens=(0, 1029, 77)),
     W.Workload("calib_g8_d128_f32", 2, 8, 1, 128, "f32", "f32", lens=(513, 1)),
     W.Workload("calib_g4_d64_bf16", 2, 8, 2, 64, "bf16", "bf16", lens=(2000, 999)),
+    # FP8 (E4M3) caches: the logits of the codes times k_scale
+    W.GQA_32K_FP8,
+    W.Workload("calib_g8_d64_e4m3_paged", 3, 16, 2, 64, "bf16", "bf16", lens=(700, 1, 33),
+               paged=True, page_size=32, kv_dtype="e4m3"),
 ]
 
 
