@@ -330,6 +330,14 @@ __device__ __forceinline__ f32x2 f2_mul(f32x2 a, f32x2 b) {
 // Two E4M3 codes (the low 16 bits of c; the lower code lands in the lower half) -> f16x2.
 // Every E4M3 value is a normal binary16 number or zero, so the conversion is exact. (A NaN
 // code converts to a NaN; caches hold none.)
+// Four E4M3 codes (bytes 0..3 of c) -> two f16x2: lo from bytes 0, 1, hi from bytes 2, 3.
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t c, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(c));
+}
+
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t c) {
   uint32_t h;
   asm("{\n\t.reg .b16 lo;\n\tcvt.u16.u32 lo, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"

@@ -456,8 +456,9 @@ __device__ __forceinline__ void mma_consume_fp8(const Params& p, MmaState<D, G>&
   float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int kk = 0; kk < KS; ++kk) {
-    const uint32_t a0 = e4m3x2_to_f16x2(k0[kk]), a2 = e4m3x2_to_f16x2(k0[kk] >> 16);
-    const uint32_t a1 = e4m3x2_to_f16x2(k1[kk]), a3 = e4m3x2_to_f16x2(k1[kk] >> 16);
+    uint32_t a0, a1, a2, a3;
+    e4m3x4_to_f16x2(k0[kk], a0, a2);
+    e4m3x4_to_f16x2(k1[kk], a1, a3);
     if (kk & 1)
       mma_f16(sb, a0, a1, a2, a3, st.qb[kk][0], st.qb[kk][1]);
     else
@@ -500,8 +501,9 @@ __device__ __forceinline__ void mma_consume_fp8(const Params& p, MmaState<D, G>&
     const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
     const uint32_t x0 = prmt(va[mt >> 1], vb[mt >> 1], sel);
     const uint32_t x1 = prmt(vc[mt >> 1], vd[mt >> 1], sel);
-    uint32_t a0 = e4m3x2_to_f16x2(x0), a1 = e4m3x2_to_f16x2(x0 >> 16);
-    uint32_t a2 = e4m3x2_to_f16x2(x1), a3 = e4m3x2_to_f16x2(x1 >> 16);
+    uint32_t a0, a1, a2, a3;
+    e4m3x4_to_f16x2(x0, a0, a1);
+    e4m3x4_to_f16x2(x1, a2, a3);
     if (tail) {
       a0 &= vm0;
       a1 &= vm0;
