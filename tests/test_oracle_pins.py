@@ -494,3 +494,29 @@ def test_fp8_scales_act_linearly():
     shape.k_scale, shape.v_scale = 0.01, 0.6
     twice_v = oracle.decode_attn(shape, q, k, v, table, sl, 0.25)
     assert np.array_equal(2.0 * base[0], twice_v[0]) and np.array_equal(base[1], twice_v[1])
+
+
+def test_oracle_rejects_bad_fp8_shapes():
+    rng = np.random.default_rng(54)
+    shape, q, k, v, table, sl = _tiny_fp8_case(rng, False, 1, 2, 1, 8, [5], 4, 0.1, 0.2)
+    for field, bad in (("kv_e4m3", 2), ("k_scale", math.nan), ("v_scale", math.inf)):
+        saved = getattr(shape, field)
+        setattr(shape, field, bad)
+        with pytest.raises(ValueError):
+            oracle.decode_attn(shape, q, k, v, table, sl, 0.5)
+        setattr(shape, field, saved)
+    oracle.decode_attn(shape, q, k, v, table, sl, 0.5)   # restored: accepted
+
+
+def test_fp8_workload_quantisation():
+    """The FP8 recipe: one scale per tensor, max |x| / 448, so the largest code is 448 and
+    code * scale stays within E4M3's half-ulp (2^-4 relative, or 2^-10 * scale absolute for
+    subnormals) of the fp32 draw."""
+    x = torch.randn((3, 40, 2, 16), generator=torch.Generator().manual_seed(5))
+    codes, scale = workloads.quantize_e4m3(x)
+    assert codes.dtype == torch.uint8 and scale == float(np.float32(x.abs().max() / 448.0))
+    vals = codes.view(torch.float8_e4m3fn).to(torch.float64)
+    assert vals.abs().max() == 448.0
+    err = (vals * scale - x.double()).abs()
+    bound = torch.maximum(x.double().abs() * 2.0 ** -4, torch.full_like(err, 2.0 ** -10 * scale))
+    assert bool((err <= bound * (1 + 1e-6)).all())
