@@ -24,6 +24,7 @@ CASES = [
     (W.GQA_32K, "sync"),
     (W.STRESS_128K, "unified"),   # flagged rows: exercises the recompute pass and its list
     (W.MHA_4K, "sync"),           # uniform splits (the plan's default for this workload)
+    (W.PAGED_B64_FP8, "unified_local"),   # an FP8 cache
 ]
 
 
