@@ -2,15 +2,18 @@
 """Benchmark: decode-attention KV-read throughput on one GB300 per rank.
 
 A step is one decode_attn_run (the split kernel with its in-kernel LSE merge and range check,
-plus in unified mode the recompute launch for flagged groups) over the named workload, inputs resident in HBM. Default workload: long-context GQA, batch
-1, 32 query heads over 8 KV heads, head_dim 128, 32768 tokens, bf16 K/V, unified-max
-softmax with the heuristic (balanced) split. Before every timed step, outside the timed
+plus in unified mode the recompute launch for flagged groups) over the named workload, inputs
+resident in HBM. Default workload: long-context GQA, batch 1, 32 query heads over 8 KV heads,
+head_dim 128, 32768 tokens, bf16 K/V, unified-max softmax with the heuristic (balanced)
+split. Other workloads: tiny, mha, paged, stress, and gqa32k_fp8 / paged_fp8 (the same
+draws over FP8 E4M3 caches). Before every timed step, outside the timed
 events, the L2 is flushed: 256 MiB are written, then 256 MiB of another buffer are read so
 that the written lines are evicted before the step rather than during it; a device-side spin
 then gives the host time to enqueue the step before the GPU reaches its start event.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--mode MODE]
   python bench.py --impl reference ...   # the float64 CPU oracle on the host cores
+  python bench.py --op logit_histogram --workload NAME   # the phi calibration pass
 
 Under torchrun each rank runs an independent replica of the workload on its own GPU
 (weak scaling); value = all ranks' KV bytes / the slowest rank's time.
