@@ -4,6 +4,7 @@ Plans are made with an explicit SM count (da_problem.num_sms), so planning never
 device, and every run below fails argument validation before anything is enqueued.
 """
 import ctypes
+import os
 import math
 
 import numpy as np
@@ -237,3 +238,27 @@ def test_kv_cache_bytes_per_token_matches_the_handbook():
     wl = workloads.GQA_32K.replace(seq_len=1)
     inp = workloads.generate(wl)
     assert inp.kv_bytes() * 32 == 128 * 1024
+
+
+def test_plain_c_program_uses_the_abi(L, tmp_path):
+    """tests/c_abi_host.c, compiled with gcc against include/decode_attn.h alone and linked to
+    the library: the boundary needs neither Python nor CUDA headers on the caller's side."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    here = os.path.dirname(os.path.abspath(__file__))
+    lib = binding.library_path()
+    exe = str(tmp_path / "c_abi_host")
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I" + lib_build.INCLUDE,
+                    os.path.join(here, "c_abi_host.c"), lib, "-Wl,-rpath," + os.path.dirname(lib),
+                    "-o", exe], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stdout + r.stderr
+    lines = r.stdout.splitlines()
+    assert lines[-1] == "ok"
+    bf16 = next(x for x in lines if x.startswith("bf16 ")).split()
+    fp8 = next(x for x in lines if x.startswith("fp8 ")).split()
+    assert int(bf16[2]) == int(fp8[2]) == 152                # grid_ctas
+    assert int(fp8[4]) >= int(bf16[4])                       # stages: FP8 tiles are smaller
