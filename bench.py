@@ -48,11 +48,14 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gqa32k")
-    ap.add_argument("--mode", default="unified", choices=["unified", "sync", "unified_local"])
+    ap.add_argument("--mode", default="unified_local",
+                    choices=["unified", "sync", "unified_local"])
     ap.add_argument("--num-splits", type=int, default=-1,
                     help="-1: the plan's heuristic; >0 uniform splits")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-side", action="store_true",
+                    help="time only the named workload (no paged / MHA / stress / FP8 lines)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--op", default="attention", choices=["attention", "logit_histogram"],
                     help="attention: the decode step (default); logit_histogram: the phi "
@@ -220,17 +223,119 @@ class L2Flush:
         self.r.max()
 
 
-def make_attn(binding, _parity, inp, mode, num_splits):
-    plan_splits = 0 if num_splits < 0 else num_splits
-    return binding.DecodeAttention(_parity.problem_for(inp, mode=mode), plan_splits)
+def pct(xs, q):
+    """The q-quantile of xs (nearest rank)."""
+    ys = sorted(xs)
+    return ys[min(len(ys) - 1, max(0, int(round(q * (len(ys) - 1)))))]
+
+
+def spread(ms_list):
+    """median / min / p90 / mean of per-step times, in µs."""
+    us = [1e3 * m for m in ms_list]
+    return {"median": round(statistics.median(us), 3), "min": round(min(us), 3),
+            "p90": round(pct(us, 0.9), 3), "mean": round(sum(us) / len(us), 3)}
+
+
+def time_step(attn, dev, wl, num_splits, steps, warmup, stream, flush, out, lse, flags,
+              sampler=None):
+    """Time `steps` decode steps (each after an L2 flush and a host-ahead spin) with CUDA
+    events around the whole step, then the same steps again with events recorded by the
+    library around the split kernel alone. Returns (step ms list, split-kernel ms list,
+    clocks)."""
+    import torch
+
+    def step(split_events=None):
+        attn.run(dev.q, dev.k, dev.v, dev.bt, dev.sl, wl.scale, num_splits, out=out,
+                 out_lse=lse, row_flags=flags, stream=stream, split_events=split_events)
+
+    for _ in range(max(3, warmup)):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    clocks = None
+    if sampler is not None:
+        sampler.start()
+    for i in range(steps):
+        flush()
+        torch.cuda._sleep(HOST_AHEAD_CYCLES)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if sampler is not None:
+        clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    ks = [RawEvent() for _ in range(steps)]
+    ke = [RawEvent() for _ in range(steps)]
+    for i in range(steps):
+        flush()
+        torch.cuda._sleep(HOST_AHEAD_CYCLES)
+        step(split_events=(ks[i], ke[i]))
+    torch.cuda.synchronize()
+    kern_ms = [a.elapsed_ms(b) for a, b in zip(ks, ke)]
+    return step_ms, kern_ms, clocks
+
+
+def launches_per_step(mode):
+    return 2 if mode == "unified" else 1   # split kernel (+ the recompute launch)
+
+
+# Workloads measured beside the headline by the default run: the other named configurations
+# of the gate and the stress test's fallback rates (paged batch, Llama2-7B-shaped MHA, the
+# unified-max stress in both unified modes), plus the FP8 caches.
+SIDE_WORKLOADS = [("mha", "unified_local"), ("paged", "unified_local"), ("stress", "unified"),
+                  ("stress", "unified_local"), ("gqa32k_fp8", "unified_local"),
+                  ("paged_fp8", "unified_local")]
+
+
+def measure_side(name, mode, args, dev_name, stream, flush, peak, peak_kind):
+    """One side workload: step and split-kernel time spread, GB/s, roofline and fallback rates."""
+    import torch
+    from decode_attention_attn_gb300 import binding, harness, workloads
+    wl = workloads.get(name).replace(mode=mode)
+    inp = workloads.generate(wl)
+    kv_bytes = inp.kv_bytes()
+    dev = harness.DeviceInputs(inp, dev_name)
+    attn = binding.DecodeAttention(harness.problem_for(inp, mode=mode), wl.num_splits)
+    B, H, d = wl.batch, wl.num_q_heads, wl.head_dim
+    out = torch.empty((B, H, d), dtype=workloads.TORCH_DTYPES[wl.out_dtype], device=dev_name)
+    lse = torch.empty((B, H), dtype=torch.float32, device=dev_name)
+    flags = torch.empty((B, H), dtype=torch.uint8, device=dev_name)
+    steps = max(10, min(args.steps, 30))
+    step_ms, kern_ms, clocks = time_step(attn, dev, wl, -1, steps, args.warmup, stream, flush,
+                                         out, lse, flags, ClockSampler(torch.cuda.current_device()))
+    stats = attn.run(dev.q, dev.k, dev.v, dev.bt, dev.sl, wl.scale, -1, want_stats=True)[3]
+    ms = statistics.median(step_ms)
+    km = statistics.median(kern_ms)
+    res = {"workload": wl.name, "softmax": mode, "kv_dtype": wl.kv_storage,
+           "kv_bytes_per_step": kv_bytes, "us_per_step": spread(step_ms),
+           "value": round(kv_bytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+           "pct_hbm_peak": round(100 * kv_bytes / (ms * 1e-3) / 1e9 / peak, 2),
+           "roofline": {"bound": "hbm", "achieved": round(kv_bytes / (km * 1e-3) / 1e9, 1),
+                        "peak": peak, "unit": "GB/s",
+                        "frac": round(kv_bytes / (km * 1e-3) / 1e9 / peak, 4),
+                        "peak_source": f"{peak_kind} hbm_gbs", "kernel": "decode_split_kernel",
+                        "kernel_us": spread(kern_ms),
+                        "traffic": profiled_traffic(wl.name)},
+           "clocks": clocks, "steps": steps, "gpu_launches": launches_per_step(mode) * steps,
+           "grid_ctas": attn.info.grid_ctas,
+           "split_tokens": [stats.split_tokens_min, stats.split_tokens]}
+    if mode != "sync":
+        rows = B * H
+        res["rows_flagged"] = int(stats.rows_flagged)
+        res["row_fallback_rate"] = round(stats.rows_flagged / rows, 6)
+        res["splits_flagged"] = int(stats.splits_flagged)
+    del dev, attn, inp, out, lse, flags
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_ours(args):
     import torch
     import torch.distributed as dist
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    import _parity
-    from decode_attention_attn_gb300 import binding, workloads
+    from decode_attention_attn_gb300 import binding, harness, workloads
 
     rank, world, local = dist_env()
     if world > 1:
@@ -241,8 +346,9 @@ def run_ours(args):
     wl = wl.replace(mode=args.mode)
     inp = workloads.generate(wl, offset=rank)
     kv_bytes = inp.kv_bytes()
-    dev = _parity.DeviceInputs(inp, dev_name)
-    attn = make_attn(binding, _parity, inp, args.mode, args.num_splits)
+    dev = harness.DeviceInputs(inp, dev_name)
+    plan_splits = 0 if args.num_splits < 0 else args.num_splits
+    attn = binding.DecodeAttention(harness.problem_for(inp, mode=args.mode), plan_splits)
     stream = torch.cuda.current_stream()
     flush = L2Flush(dev_name)
     B, H, d = wl.batch, wl.num_q_heads, wl.head_dim
@@ -250,49 +356,19 @@ def run_ours(args):
     lse = torch.empty((B, H), dtype=torch.float32, device=dev_name)
     flags = torch.empty((B, H), dtype=torch.uint8, device=dev_name)
 
-    def step(events=None, split_events=None):
-        attn.run(dev.q, dev.k, dev.v, dev.bt, dev.sl, wl.scale, args.num_splits, out=out,
-                 out_lse=lse, row_flags=flags, stream=stream, split_events=split_events)
-
-    for _ in range(max(3, args.warmup)):
-        flush()
-        step()
-    torch.cuda.synchronize()
-
-    # ---- timed region: whole steps ----
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    sampler = ClockSampler(local)
+    # ---- timed region: whole steps; then the split kernel alone, same steps and flushes ----
     if world > 1:
         dist.barrier()
-    torch.cuda.synchronize()
-    sampler.start()
     t_wall0 = time.perf_counter()
-    for i in range(args.steps):
-        flush()
-        torch.cuda._sleep(HOST_AHEAD_CYCLES)
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
-    torch.cuda.synchronize()
+    step_ms, kern_ms, clocks = time_step(attn, dev, wl, args.num_splits, args.steps, args.warmup,
+                                         stream, flush, out, lse, flags, ClockSampler(local))
     t_wall = time.perf_counter() - t_wall0
-    clocks = sampler.stop()
     if world > 1:
         dist.barrier()
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms_local = sum(step_ms) / len(step_ms)
-
-    # ---- split kernel alone (events recorded around its launch), same steps and flushes ----
-    ks = [RawEvent() for _ in range(args.steps)]
-    ke = [RawEvent() for _ in range(args.steps)]
-    for i in range(args.steps):
-        flush()
-        torch.cuda._sleep(HOST_AHEAD_CYCLES)
-        step(split_events=(ks[i], ke[i]))
-    torch.cuda.synchronize()
-    kern_ms = sum(s.elapsed_ms(e) for s, e in zip(ks, ke)) / args.steps
-
-    ms, kern_ms = max_over_ranks([ms_local, kern_ms], dev_name)
+    ms, kern_med = max_over_ranks([statistics.median(step_ms), statistics.median(kern_ms)],
+                                  dev_name)
+    stats = attn.run(dev.q, dev.k, dev.v, dev.bt, dev.sl, wl.scale, args.num_splits,
+                     want_stats=True)[3]
 
     # ---- end to end: pinned host inputs -> device -> run -> host results ----
     e2e = None
@@ -319,17 +395,25 @@ def run_ours(args):
             dev.sl.copy_(hsl, non_blocking=True)
             if hbt is not None:
                 dev.bt.copy_(hbt, non_blocking=True)
-            step()
+            attn.run(dev.q, dev.k, dev.v, dev.bt, dev.sl, wl.scale, args.num_splits, out=out,
+                     out_lse=lse, row_flags=flags, stream=stream)
             hout.copy_(out, non_blocking=True)
             hlse.copy_(lse, non_blocking=True)
             if j >= 0:
                 ee[j].record(stream)
             stream.synchronize()
-        e2e_ms = sum(s.elapsed_time(e) for s, e in zip(es, ee)) / e_steps
+        e2e_ms = statistics.median([a.elapsed_time(b) for a, b in zip(es, ee)])
         e2e_ms = max_over_ranks([e2e_ms], dev_name)[0]
         e2e = {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": round(e2e_ms, 4)}
+
+    peak, peak_kind = measured_peaks()
+    side = []
+    if rank == 0 and world == 1 and not args.no_side and args.workload == "gqa32k" \
+            and args.num_splits < 0:
+        side = [measure_side(n, m, args, dev_name, stream, flush, peak, peak_kind)
+                for n, m in SIDE_WORKLOADS]
 
     if world > 1:
         dist.barrier()
@@ -338,10 +422,8 @@ def run_ours(args):
             dist.destroy_process_group()
         return
 
-    peak, peak_kind = measured_peaks()
-    achieved = kv_bytes / (kern_ms * 1e-3) / 1e9
+    achieved = kv_bytes / (kern_med * 1e-3) / 1e9
     value = world * kv_bytes / (ms * 1e-3) / 1e9
-    launches_per_step = 2 if args.mode == "unified" else 1   # split (+ recompute launch)
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -350,7 +432,7 @@ def run_ours(args):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(ms, 5),
-        "us_per_step": round(ms * 1e3, 2),
+        "us_per_step": spread(step_ms),
         "pct_hbm_peak": round(100 * value / world / peak, 2),
         "higher_is_better": True,
         "scaling": "weak",
@@ -363,20 +445,27 @@ def run_ours(args):
                    "out_dtype": wl.out_dtype, "softmax": args.mode,
                    "splits": "heuristic (balanced shares)" if args.num_splits < 0 else args.num_splits,
                    "grid_ctas": attn.info.grid_ctas, "stages": attn.info.stages,
+                   "split_tokens": [stats.split_tokens_min, stats.split_tokens],
                    "kv_bytes_per_step": kv_bytes,
+                   "timing": "value and ms_per_step from the median step; us_per_step gives median, min, p90 and mean",
                    "l2": f"flushed before every timed step: {FLUSH_BYTES >> 20} MiB written, then {FLUSH_BYTES >> 20} MiB of another buffer read (evicts the dirty lines)",
                    "host_ahead": f"a {HOST_AHEAD_CYCLES}-cycle device spin precedes each timed step, outside its events, so host call overhead is not timed as device time (e2e times it)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"{peak_kind} hbm_gbs",
-                     "kernel": "decode_split_kernel", "kernel_ms": round(kern_ms, 5),
+                     "kernel": "decode_split_kernel", "kernel_us": spread(kern_ms),
                      "traffic": profiled_traffic(wl.name)},
         "clocks": clocks,
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": launches_per_step(args.mode) * args.steps,
         "e2e": e2e,
         "wall_s_timed": round(t_wall, 3),
     }
+    if args.mode != "sync":
+        line["rows_flagged"] = int(stats.rows_flagged)
+        line["splits_flagged"] = int(stats.splits_flagged)
+    if side:
+        line["workloads"] = side
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds, out)
     print(json.dumps(line), flush=True)
@@ -385,28 +474,38 @@ def run_ours(args):
 
 
 def cpu_baseline(inp, seconds, out=None):
-    """The float64 CPU oracle, as it stands, on this host's cores over the same inputs. When
-    `out` (the GPU result of the timed launch configuration on these inputs) is given, the
-    oracle's result also checks it, within the parity tolerance."""
+    """The float64 CPU oracle, as it stands, on this host's cores over the same inputs: with
+    one thread per host core (the headline baseline) and with a single thread. When `out`
+    (the GPU result of the timed launch configuration on these inputs) is given, the oracle's
+    result also checks it, within the parity tolerance."""
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     import _parity
     import oracle
     threads = oracle.host_threads()
     rows = inp.wl.batch * inp.wl.num_q_heads
-    t0 = time.perf_counter()
-    n = 0
-    while True:
-        ref = _parity.run_oracle(inp, nthreads=threads)[0]
-        n += 1
-        if time.perf_counter() - t0 >= seconds:
-            break
-    dt = (time.perf_counter() - t0) / n
+
+    def timed(nthreads, budget):
+        t0 = time.perf_counter()
+        n = 0
+        ref = None
+        while True:
+            ref = _parity.run_oracle(inp, nthreads=nthreads)[0]
+            n += 1
+            if time.perf_counter() - t0 >= budget:
+                break
+        return (time.perf_counter() - t0) / n, n, ref
+
+    dt, n, ref = timed(threads, seconds)
     if out is not None:
         _parity.compare(out, ref, inp.wl.out_dtype, where="bench output vs oracle")
+    dt1, n1, _ = timed(1, seconds / 2)
     return {"value": round(inp.kv_bytes() / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
             "kind": "oracle", "ms_per_step": round(dt * 1e3, 2),
             "sample": f"the whole workload ({rows} query rows, every token), {n} passes",
-            "checked_gpu_output": out is not None}
+            "checked_gpu_output": out is not None,
+            "single_thread": {"value": round(inp.kv_bytes() / dt1 / 1e9, 4), "unit": "GB/s",
+                              "cores": 1, "ms_per_step": round(dt1 * 1e3, 2),
+                              "sample": f"the whole workload, {n1} passes"}}
 
 
 def run_reference(args):
@@ -483,9 +582,7 @@ def run_histogram(args):
     launch per step over the workload's K, L2 flushed before each step."""
     import numpy as np
     import torch
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    import _parity
-    from decode_attention_attn_gb300 import binding, workloads
+    from decode_attention_attn_gb300 import binding, harness, workloads
 
     rank, world, local = dist_env()
     if world > 1:
@@ -495,8 +592,8 @@ def run_histogram(args):
     wl = workloads.get(args.workload)
     inp = workloads.generate(wl)
     k_bytes = inp.kv_bytes() // 2
-    dev = _parity.DeviceInputs(inp)
-    attn = binding.DecodeAttention(_parity.problem_for(inp, mode="sync"), 0)
+    dev = harness.DeviceInputs(inp)
+    attn = binding.DecodeAttention(harness.problem_for(inp, mode="sync"), 0)
     stream = torch.cuda.current_stream()
     flush = L2Flush(f"cuda:{local}")
     counts = torch.zeros(HIST_BINS + 2, dtype=torch.int64, device=f"cuda:{local}")
