@@ -69,6 +69,8 @@ class da_plan_info(ctypes.Structure):
         ("max_splits", ctypes.c_int),
         ("workspace_bytes", ctypes.c_size_t),
         ("smem_bytes", ctypes.c_size_t),
+        ("split_tokens", ctypes.c_int),
+        ("split_tokens_min", ctypes.c_int),
     ]
 
 
@@ -79,6 +81,8 @@ class da_stats(ctypes.Structure):
         ("rows_flagged", ctypes.c_longlong),
         ("splits_flagged", ctypes.c_longlong),
         ("recompute_launched", ctypes.c_int),
+        ("split_tokens", ctypes.c_int),
+        ("split_tokens_min", ctypes.c_int),
     ]
 
 

@@ -16,6 +16,7 @@
 #include <utility>
 
 #include "da_device.cuh"
+#include "da_scratch_cache.h"
 
 namespace da {
 const void* kernel_f32(int head_dim, int group, int mode);
@@ -229,6 +230,7 @@ struct da_plan {
   int group, es, unit, box_tokens, capacity, n_groups, piece_units;
   int kv_es;                    // K / V bytes per element (1: FP8 E4M3 cache; else es)
   int policy, num_splits;       // the plan's default split choice
+  int narrow;                   // the device schedule's arithmetic fits 32 bits
   int grid;                     // balanced grid (or the default uniform grid)
   int recompute_splits, max_splits;
   int stages, batch_smem;
@@ -444,6 +446,7 @@ void fill_common(const da_plan& pl, Params& k, const int32_t* block_table,
   k.n_groups = pl.n_groups;
   k.stages = pl.stages;
   k.batch_smem = pl.batch_smem;
+  k.narrow = pl.narrow;
 }
 
 int status_to_error(int s) {
@@ -542,6 +545,15 @@ int decode_attn_plan(const da_problem* problem, int num_splits, da_plan** plan_o
       (long long)pl->n_groups * std::max(pl->recompute_splits, pl->policy == kUniform ? pl->num_splits : 1);
   pl->slots = std::max<long long>((long long)sms + pl->n_groups, need_uniform);
   pl->max_splits = (int)std::min<long long>(split_cap, pl->slots / pl->n_groups);
+  {
+    // the largest unit index (balanced) or item count (uniform splits, any num_splits up to
+    // max_splits, and the recompute pass) times the CTA count must stay below 2^31 for the
+    // device's 32-bit schedule arithmetic
+    const long long units = (long long)pl->n_groups * (units_max + pl->piece_units);
+    const long long items = (long long)pl->n_groups * std::max(pl->max_splits, pl->recompute_splits);
+    const long long ctas = std::max<long long>(sms, 1);
+    pl->narrow = (units + 1) * ctas < (1ll << 31) && (items + 1) * ctas < (1ll << 31) ? 1 : 0;
+  }
 
   // deepest pipeline that fits the per-CTA shared memory limit
   pl->stages = 0;
@@ -558,6 +570,8 @@ int decode_attn_plan(const da_problem* problem, int num_splits, da_plan** plan_o
     return DA_ERR_UNSUPPORTED;
   }
 
+  // Workspace: the counters, the flagged list, status and statistics (zeroed once, left at
+  // zero by every run), then the partials (no initial value needed).
   const int G = pl->group, D = p.head_dim;
   size_t off = 0;
   pl->off_counters = off;
@@ -566,8 +580,8 @@ int decode_attn_plan(const da_problem* problem, int num_splits, da_plan** plan_o
   off = align256(off + (size_t)pl->n_groups * 4);
   pl->off_list_state = off;      // 2 x int32
   pl->off_status = off + 16;     // int32
-  pl->off_stats = off + 24;      // 2 x uint64
-  off = align256(off + 40);
+  pl->off_stats = off + 24;      // 4 x uint64
+  off = align256(off + 56);
   pl->zero_bytes = off;
   pl->off_part_flags = off;
   off = align256(off + (size_t)pl->slots * 4);
@@ -582,8 +596,44 @@ int decode_attn_plan(const da_problem* problem, int num_splits, da_plan** plan_o
   return DA_OK;
 }
 
+// Largest and smallest piece (tokens) of a step whose sequences are all at capacity, under
+// the plan's default policy: the host-side image of the device's schedule.
+void full_step_pieces(const da_plan& pl, int* mx, int* mn) {
+  const long long cap = pl.capacity, unit = pl.unit;
+  long long hi = 0, lo = 0;
+  if (pl.policy == kUniform) {
+    const long long S = pl.num_splits;
+    const long long ts = ((cap + S - 1) / S + unit - 1) / unit * unit;
+    hi = std::min(ts, cap);
+    lo = cap - (S - 1) * ts > 0 ? std::min(hi, cap - (S - 1) * ts) : 0;
+    for (long long sp = 0; sp < S; ++sp) {   // splits past the end are empty
+      const long long t0 = std::min(cap, sp * ts), t1 = std::min(cap, t0 + ts);
+      lo = sp == 0 ? t1 - t0 : std::min(lo, t1 - t0);
+    }
+  } else {
+    const long long per = (cap + unit - 1) / unit + pl.piece_units;
+    const long long W = (long long)pl.n_groups * per;
+    const long long P = std::min<long long>(pl.grid, W);
+    lo = cap;
+    for (long long c = 0; c < P; ++c) {
+      const long long u0 = c * W / P, u1 = (c + 1) * W / P;
+      for (long long g = u0 / per; g * per < u1 && g < pl.n_groups; ++g) {
+        const long long rs = g * per + pl.piece_units, ge = (g + 1) * per;
+        const long long a = std::max(u0, rs), b = std::min(u1, ge);
+        if (b <= a) continue;
+        const long long t = std::min(cap, (b - rs) * unit) - (a - rs) * unit;
+        hi = std::max(hi, t);
+        lo = std::min(lo, t);
+      }
+    }
+  }
+  *mx = (int)hi;
+  *mn = (int)lo;
+}
+
 int decode_attn_plan_info(const da_plan* plan, da_plan_info* info) {
   if (!plan || !info) return DA_ERR_INVALID_ARG;
+  full_step_pieces(*plan, &info->split_tokens, &info->split_tokens_min);
   info->grid_ctas = plan->grid;
   info->num_splits = plan->policy == kBalanced ? 0 : plan->num_splits;
   info->unit_tokens = plan->unit;
@@ -701,10 +751,11 @@ int decode_attn_run_ex(const da_plan* plan, const da_run_args* args) {
                        : uniform_grid((long long)pl.n_groups * S, pl.num_sms);
 
   const bool sync_after = stats != nullptr || p.validate;
+  kp.piece_stats = stats != nullptr ? 1 : 0;
   char* ws = static_cast<char*>(workspace);
   cudaError_t e;
   if (sync_after) {
-    e = cudaMemsetAsync(ws + pl.off_status, 0, 24, stream);   // status + stats counters
+    e = cudaMemsetAsync(ws + pl.off_status, 0, 40, stream);   // status + stats counters
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(status)");
   }
 
@@ -738,6 +789,7 @@ int decode_attn_run_ex(const da_plan* plan, const da_run_args* args) {
     rp.policy = kUniform;
     rp.num_splits = pl.recompute_splits;
     rp.recompute = 1;
+    rp.piece_stats = 0;
     const void* rfn = kernel_for(pl, DA_SOFTMAX_SYNC);
     rc = ensure_smem_attr(rfn, pl.smem_bytes);
     if (rc != DA_OK) return rc;
@@ -756,10 +808,10 @@ int decode_attn_run_ex(const da_plan* plan, const da_run_args* args) {
 
   if (sync_after) {
     int32_t st = 0;
-    unsigned long long counts[2] = {0, 0};
+    unsigned long long counts[4] = {0, 0, 0, 0};
     e = cudaMemcpyAsync(&st, ws + pl.off_status, 4, cudaMemcpyDeviceToHost, stream);
     if (e == cudaSuccess)
-      e = cudaMemcpyAsync(counts, ws + pl.off_stats, 16, cudaMemcpyDeviceToHost, stream);
+      e = cudaMemcpyAsync(counts, ws + pl.off_stats, 32, cudaMemcpyDeviceToHost, stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_fail(e, "reading the device status");
     if (stats) {
@@ -768,6 +820,8 @@ int decode_attn_run_ex(const da_plan* plan, const da_run_args* args) {
       stats->rows_flagged = (long long)counts[0];
       stats->splits_flagged = (long long)counts[1];
       stats->recompute_launched = unified ? 1 : 0;
+      stats->split_tokens = (int)counts[2];
+      stats->split_tokens_min = counts[3] ? (int)(0x7fffffffull - counts[3]) : 0;
     }
     const int err = status_to_error(st);
     if (err != DA_OK) return err;
@@ -891,27 +945,63 @@ static __device__ __align__(256) unsigned char g_static_scratch[DECODE_ATTN_STAT
 
 namespace {
 
-constexpr int kMaxStaticDevices = 64;
-std::mutex g_static_mu;
-void* g_static_addr[kMaxStaticDevices] = {};
+SymbolAddressCache<64> g_static_cache;
 
-// Device address of the current device's scratch region. Looked up on the first call made
-// with that device current (which loads the library's device code there if it is not yet
-// loaded) and cached for later calls.
-int static_scratch(void** addr) {
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= kMaxStaticDevices) return DA_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_static_mu);
-  if (!g_static_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
-    g_static_addr[dev] = p;
+// Unique ID of the calling thread's current CUDA context (0 when none is current yet).
+int current_context_id(unsigned long long* id) {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* a = nullptr;
+    void* b = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 4000, cudaEnableDefault, &q1) ==
+            cudaSuccess && q1 == cudaDriverEntryPointSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &q2) ==
+            cudaSuccess && q2 == cudaDriverEntryPointSuccess) {
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(a);
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(b);
+    }
+  });
+  if (!get_current || !get_id) {
+    g_cuda_error = "cuCtxGetCurrent / cuCtxGetId are not available from the driver";
+    return DA_ERR_CUDA;
   }
-  *addr = g_static_addr[dev];
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) {
+    g_cuda_error = "cuCtxGetCurrent failed";
+    return DA_ERR_CUDA;
+  }
+  *id = 0;
+  if (ctx && get_id(ctx, id) != CUDA_SUCCESS) {
+    g_cuda_error = "cuCtxGetId failed";
+    return DA_ERR_CUDA;
+  }
   return DA_OK;
+}
+
+// Device address of the scratch region in the calling thread's current context. Looked up
+// (cudaGetSymbolAddress, which loads the library's device code into the context if needed)
+// on the first call in each context and cached under the context's unique ID, so a device
+// reset or a caller's own driver context gets its own lookup.
+int static_scratch(void** addr) {
+  auto resolve = [](void** out) -> int {
+    const cudaError_t e = cudaGetSymbolAddress(out, g_static_scratch);
+    return e == cudaSuccess ? DA_OK : cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+  };
+  unsigned long long id = 0;
+  int rc = current_context_id(&id);
+  if (rc != DA_OK) return rc;
+  if (id == 0) {
+    // no context is current yet: the lookup makes the device's primary context current
+    rc = resolve(addr);
+    if (rc != DA_OK) return rc;
+    rc = current_context_id(&id);
+    if (rc != DA_OK) return rc;
+    if (id == 0) return DA_OK;   // (not cached)
+  }
+  return g_static_cache.get(id, resolve, addr);
 }
 
 // decode_attn_run's host-side argument checks, made before the scratch is cleared so that
@@ -928,6 +1018,9 @@ int static_args_ok(const da_plan& pl, const void* q, const void* k_cache, const 
   if (!std::isfinite(scale) || num_splits < -1) return DA_ERR_INVALID_ARG;
   if (num_splits == 0 && pl.batch_smem == 0) return DA_ERR_UNSUPPORTED;
   if (num_splits > pl.max_splits) return DA_ERR_WORKSPACE_TOO_SMALL;
+  if (!kernel_for(pl, pl.prob.mode)) return DA_ERR_UNSUPPORTED;
+  if (pl.prob.mode == DA_SOFTMAX_UNIFIED && !kernel_for(pl, DA_SOFTMAX_SYNC))
+    return DA_ERR_UNSUPPORTED;
   return DA_OK;
 }
 

@@ -71,7 +71,8 @@ struct Params {
   int32_t* list_state;           // unified: [0] flagged count, [1] recompute CTAs finished
                                  // (self-cleaning)
   int32_t* status;               // device findings
-  unsigned long long* stats;     // [0] rows flagged, [1] split partials flagged
+  unsigned long long* stats;     // [0] rows flagged, [1] split partials flagged, [2] largest
+                                 // piece (tokens), [3] 2^31 - 1 - smallest piece (tokens)
   uint32_t* part_flags;          // [slots] range-check bits per head
   float* part_l;                 // [slots, G] log2-domain LSE of each partial
   float* part_o;                 // [slots, G, D] normalised partial outputs
@@ -87,6 +88,9 @@ struct Params {
   int num_splits;                // uniform: splits per group
   int recompute;                 // 1: the recompute launch (groups from the flagged list)
   int list_flags;                // 1: flagged groups go to the list (a recompute launch follows)
+  int piece_stats;               // 1: record the largest and smallest piece in stats[2..3]
+  int narrow;                    // 1: every product of the schedule's unit / item arithmetic
+                                 // (index x CTA count) is below 2^31: 32-bit division suffices
   int n_groups;                  // B * Hkv
   int stages;                    // pipeline depth
   int batch_smem;                // lengths held in smem (balanced) or 0

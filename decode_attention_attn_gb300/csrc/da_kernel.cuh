@@ -88,51 +88,62 @@ __device__ __forceinline__ int clamp_len(const Params& p, int n) {
   return n < 0 ? 0 : (n > p.capacity ? p.capacity : n);
 }
 
-// CTA whose balanced share [floor(c W / P), floor((c + 1) W / P)) holds unit u.
-__device__ __forceinline__ long long cta_of(long long u, long long W, int P) {
+// CTA whose balanced share [floor(c W / P), floor((c + 1) W / P)) holds unit u. I is the
+// integer type of the unit space: 32-bit when the host found every product below 2^31 (no
+// calls to the 64-bit division routine on the paths that start the step), else 64-bit.
+template <typename I>
+__device__ __forceinline__ I cta_of(I u, I W, I P) {
   return ((u + 1) * P - 1) / W;
 }
 
-__device__ __forceinline__ bool sched_next(Sched& s, const Params& p, Piece& pc) {
-  if (s.policy == kBalanced) {
-    // Group g of sequence b owns units [gs, ge) of the step's unit space: piece_units cost
-    // units, then one per `unit` tokens. A share that holds only cost units of a group has no
-    // piece of it.
-    while (s.u < s.u1) {
-      const long long u = s.u;
-      const long long hkv = p.hkv;
-      int lo = 0, hi = p.batch;   // invariant: hkv * prefix[lo] <= u < hkv * prefix[hi]
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (hkv * s.prefix[mid] <= u) lo = mid; else hi = mid;
-      }
-      const int b = lo;
-      const long long nb = s.prefix[b + 1] - s.prefix[b];
-      const long long base = hkv * s.prefix[b];
-      const int kvh = (int)((u - base) / nb);
-      const long long gs = base + kvh * nb, ge = gs + nb;
-      const long long rs = gs + p.piece_units;   // the group's first token unit
-      const long long pe = s.u1 < ge ? s.u1 : ge;
-      s.u = pe;
-      if (pe <= rs) continue;
-      const long long n = s.lens[b];
-      pc.b = b;
-      pc.kvh = kvh;
-      pc.g = b * p.hkv + kvh;
-      pc.t0 = (int)(((u > rs ? u : rs) - rs) * p.unit);
-      const long long t1 = (pe - rs) * p.unit;
-      pc.t1 = (int)(t1 < n ? t1 : n);
-      const long long cf = cta_of(rs, s.W, s.P), cl = cta_of(ge - 1, s.W, s.P);
-      pc.nslots = (int)(cl - cf + 1);
-      pc.slot_base = (int)cf + pc.g;
-      pc.slot = s.c + pc.g;
-      return true;
+// Balanced shares. Group g of sequence b owns units [gs, ge) of the step's unit space:
+// piece_units cost units, then one per `unit` tokens. A share that holds only cost units of a
+// group has no piece of it.
+template <typename I>
+__device__ __forceinline__ bool sched_balanced(Sched& s, const Params& p, Piece& pc) {
+  const I u1 = (I)s.u1, W = (I)s.W, P = (I)s.P, hkv = (I)p.hkv, pu = (I)p.piece_units;
+  I u = (I)s.u;
+  while (u < u1) {
+    int lo = 0, hi = p.batch;   // invariant: hkv * prefix[lo] <= u < hkv * prefix[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (hkv * (I)s.prefix[mid] <= u) lo = mid; else hi = mid;
     }
-    return false;
+    const int b = lo;
+    const I nb = (I)(s.prefix[b + 1] - s.prefix[b]);
+    const I base = hkv * (I)s.prefix[b];
+    const int kvh = (int)((u - base) / nb);
+    const I gs = base + (I)kvh * nb, ge = gs + nb;
+    const I rs = gs + pu;   // the group's first token unit
+    const I pe = u1 < ge ? u1 : ge;
+    const I u_at = u;
+    u = pe;
+    if (pe <= rs) continue;
+    s.u = (long long)u;
+    const I n = (I)s.lens[b];
+    pc.b = b;
+    pc.kvh = kvh;
+    pc.g = b * p.hkv + kvh;
+    pc.t0 = (int)(((u_at > rs ? u_at : rs) - rs) * (I)p.unit);
+    const I t1 = (pe - rs) * (I)p.unit;
+    pc.t1 = (int)(t1 < n ? t1 : n);
+    const I cf = cta_of<I>(rs, W, P), cl = cta_of<I>(ge - 1, W, P);
+    pc.nslots = (int)(cl - cf + 1);
+    pc.slot_base = (int)cf + pc.g;
+    pc.slot = s.c + pc.g;
+    return true;
   }
+  s.u = (long long)u;
+  return false;
+}
+
+__device__ __forceinline__ bool sched_next(Sched& s, const Params& p, Piece& pc) {
+  if (s.policy == kBalanced)
+    return p.narrow ? sched_balanced<unsigned>(s, p, pc) : sched_balanced<long long>(s, p, pc);
   if (s.i >= s.i1) return false;
   const long long i = s.i++;
-  const int li = (int)(i / s.S), sp = (int)(i % s.S);
+  const int li = p.narrow ? (int)((unsigned)i / (unsigned)s.S) : (int)(i / s.S);
+  const int sp = (int)(i - (long long)li * s.S);
   const int g = s.use_list ? __ldcg(p.flag_list + li) : li;
   const int b = g / p.hkv;
   const int n = clamp_len(p, __ldg(p.seq_lens + b));
@@ -158,11 +169,13 @@ template <typename T, int D, int G, bool SWZ>
 __device__ __forceinline__ void run_producer(const Params& p, Sched s, uint8_t* stages,
                                              const Layout& L, uint64_t* full, uint64_t* empty,
                                              const CUtensorMap* tmk, const CUtensorMap* tmv,
-                                             int lane, int part, uint32_t& k, bool& dead) {
+                                             int lane, int part) {
   using C = Cfg<T, D, G>;
   const uint64_t pol = make_evict_first_policy();
   const uint32_t NS = (uint32_t)p.stages;
   const int nsub = p.paged ? 2 : 1;   // warps per tensor: K from even parts, V from odd
+  uint32_t k = 0;
+  bool dead = false;
   uint32_t issued = 0;   // one past the last stage this call issued copies for
   Piece pc;
   while (sched_next(s, p, pc)) {
@@ -589,17 +602,166 @@ __device__ __forceinline__ void publish_mma(const MmaState<D, G>& st, float m0, 
   if (lane == 0) mflag[warp] = fm;
 }
 
-// The 8 consumer warps' published states -> one partial (or the output, when the piece is
-// its group's only one). The last piece of a group to finish merges the group's partials
-// here (the split-KV log-sum-exp merge, "The Rescaling and Online Softmax Reduction
-// Algorithm"): L = log2 sum_s 2^L_s, O = sum_s 2^(L_s - L) O_s. `first_phase`: the piece
-// belongs to the step's first pass, which records flags, statistics and the flagged list.
+// Each consumer thread owns EPT consecutive output elements of one head in the combine and
+// merge steps (e0 = thread * EPT; threads with e0 >= G * D own none).
+template <int D, int G>
+struct CombineMap {
+  static constexpr int kCT = kConsumerWarps * 32;
+  static constexpr int EPT = G * D >= 4 * kCT ? 4 : (G * D >= 2 * kCT ? 2 : 1);
+  int e0, g, d0;
+  bool owns;
+  __device__ __forceinline__ explicit CombineMap(int ctid) {
+    e0 = ctid * EPT;
+    owns = e0 < G * D;
+    g = owns ? e0 / D : 0;
+    d0 = e0 - g * D;
+  }
+};
+
+template <int N>
+__device__ __forceinline__ void load_smem_vec(const float* src, float (&v)[N]) {
+  if constexpr (N == 4) {
+    const float4 x = *reinterpret_cast<const float4*>(src);
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+  } else if constexpr (N == 2) {
+    const float2 x = *reinterpret_cast<const float2*>(src);
+    v[0] = x.x; v[1] = x.y;
+  } else {
+    v[0] = src[0];
+  }
+}
+
+// The last piece of a group to finish merges it (recompute pass): the partial goes to the
+// workspace, a release-acquire arrival count picks the last piece, which loads all partials
+// and forms L = log2 sum_s 2^L_s, O = sum_s 2^(L_s - L) O_s.
+template <typename T, int D, int G>
+__device__ __forceinline__ void merge_last_arriver(const Params& p, const Piece& pc,
+                                                   bool first_phase,
+                                                   const float (&o)[CombineMap<D, G>::EPT],
+                                                   float L2, uint32_t fl, float* mm, float* ml,
+                                                   float* wbuf, int* misc, int warp, int lane,
+                                                   int ctid) {
+  using CM = CombineMap<D, G>;
+  constexpr int kCT = CM::kCT, EPT = CM::EPT;
+  constexpr float kLn2 = 0.6931471805599453f;
+  const CM cm(ctid);
+  const long long row0 = (long long)pc.b * p.hq + (long long)pc.kvh * G;
+  if (cm.owns) {
+    float* dst = p.part_o + ((long long)pc.slot * G + cm.g) * D + cm.d0;
+#pragma unroll
+    for (int i = 0; i < EPT; ++i) __stcg(dst + i, o[i]);
+    if (cm.d0 == 0) __stcg(p.part_l + (long long)pc.slot * G + cm.g, L2);
+  }
+  if (ctid == 0) __stcg(p.part_flags + pc.slot, fl);
+  // Arrival: the barrier orders the CTA's partial writes before thread 0's release-acquire
+  // count; the last piece's count also acquires the other pieces' partials.
+  named_bar_sync(1, kCT);
+  if (ctid == 0) {
+    const int old = atom_add_acq_rel_gpu(p.counters + pc.g, 1);
+    misc[0] = old == pc.nslots - 1;
+    misc[1] = 0;
+  }
+  named_bar_sync(1, kCT);
+  if (!misc[0]) return;
+  // Last piece of the group: merge all its partials; each thread issues the loads of up to 64
+  // partial values at once, together with the LSEs, so a group of up to 64 / EPT pieces pays
+  // the L2 latency once.
+  const int S = pc.nslots;
+  float* wts = wbuf;              // [S, G] weights (scratch reused; S <= 8 * D)
+  float* hsum = mm;               // [G] sum of weights
+  float* hmax = ml;               // [G] maximum partial LSE
+  constexpr int SB = 64 / EPT;
+  const float* po = p.part_o + (long long)pc.slot_base * G * D + (cm.owns ? cm.e0 : 0);
+  float ob[SB][EPT];
+  auto load_block = [&](int s0) {
+#pragma unroll
+    for (int j = 0; j < SB; ++j) {
+      const bool ok = cm.owns && s0 + j < S;
+      const float* src = po + (long long)(s0 + j) * G * D;
+#pragma unroll
+      for (int i = 0; i < EPT; ++i) ob[j][i] = ok ? __ldcg(src + i) : 0.f;
+    }
+  };
+  load_block(0);
+  const float* pl = p.part_l + (long long)pc.slot_base * G;
+  for (int i = ctid; i < S * G; i += kCT) wts[i] = __ldcg(pl + i);
+  uint32_t rf = 0;
+  for (int s = ctid; s < S; s += kCT) rf |= __ldcg(p.part_flags + pc.slot_base + s);
+  rf = __reduce_or_sync(0xffffffffu, rf);
+  if (lane == 0 && rf) atomicOr(reinterpret_cast<unsigned int*>(misc + 1), rf);
+  named_bar_sync(1, kCT);
+  if (warp < G) {
+    const int g = warp;
+    float M = -INFINITY;
+    for (int s = lane; s < S; s += 32) M = fmaxf(M, wts[s * G + g]);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float sum = 0.f;
+    for (int s = lane; s < S; s += 32) {
+      const float L = wts[s * G + g];
+      const float f = L > -INFINITY ? fast_exp2(L - M) : 0.f;
+      wts[s * G + g] = f;
+      sum += f;
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (lane == 0) {
+      hsum[g] = sum;
+      hmax[g] = M;
+    }
+  }
+  named_bar_sync(1, kCT);
+  float num[EPT];
+#pragma unroll
+  for (int i = 0; i < EPT; ++i) num[i] = 0.f;
+  for (int s0 = 0; s0 < S; s0 += SB) {
+    if (s0 > 0) load_block(s0);
+#pragma unroll
+    for (int j = 0; j < SB; ++j) {
+      if (s0 + j < S) {
+        const float w = wts[(s0 + j) * G + cm.g];
+#pragma unroll
+        for (int i = 0; i < EPT; ++i) num[i] += w * ob[j][i];
+      }
+    }
+  }
+  const uint32_t rfa = (uint32_t)misc[1];
+  if (cm.owns) {
+    const float sum = hsum[cm.g];
+#pragma unroll
+    for (int i = 0; i < EPT; ++i)
+      store_out(p.out, (row0 + cm.g) * D + cm.d0 + i, p.out_dtype,
+                sum > 0.f ? num[i] / sum * p.v_scale : 0.f);
+    if (cm.d0 == 0) {
+      if (p.out_lse)
+        p.out_lse[row0 + cm.g] = sum > 0.f ? (hmax[cm.g] + fast_log2(sum)) * kLn2 : -INFINITY;
+      if (p.row_flags && first_phase) p.row_flags[row0 + cm.g] = (uint8_t)((rfa >> cm.g) & 1u);
+    }
+  }
+  if (ctid == 0) {
+    p.counters[pc.g] = 0;   // leave the counter ready for the next run
+    if (first_phase && rfa) {
+      atomicAdd(p.stats + 0, (unsigned long long)__popc(rfa));
+      if (p.list_flags) {
+        const int at = atomicAdd(p.list_state, 1);
+        if (at < p.n_groups) p.flag_list[at] = pc.g;
+      }
+    }
+  }
+}
+
+// The 8 consumer warps' published states -> one partial of the piece (or the output, when the
+// piece is its group's only one), then the group's merge where this piece takes part in it
+// (the split-KV log-sum-exp merge, "The Rescaling and Online Softmax Reduction Algorithm").
+// `first_phase`: the piece belongs to the step's first pass, which records flags, statistics
+// and the flagged list.
 template <typename T, int D, int G>
 __device__ __forceinline__ void combine_piece(const Params& p, const Piece& pc, bool first_phase,
                                               float* mm, float* ml, uint32_t* mflag,
                                               float* wbuf, int* misc, int warp, int lane,
                                               int ctid) {
-  constexpr int kCT = kConsumerWarps * 32;
+  using CM = CombineMap<D, G>;
+  constexpr int kCT = CM::kCT, EPT = CM::EPT;
   constexpr float kLn2 = 0.6931471805599453f;
   constexpr int W = warp_scratch_floats(D, G, Cfg<T, D, G>::kQEs);
   named_bar_sync(1, kCT);
@@ -609,162 +771,68 @@ __device__ __forceinline__ void combine_piece(const Params& p, const Piece& pc, 
   for (int w = 0; w < kConsumerWarps; ++w) fl |= mflag[w];
   const bool direct = pc.nslots == 1;
   const long long row0 = (long long)pc.b * p.hq + (long long)pc.kvh * G;
+  const CM cm(ctid);
 
-  // the 8 warps' (m, l, acc) -> one partial: max-rescale merge within the CTA
-  for (int e = ctid; e < G * D; e += kCT) {
-    const int g = e / D, d = e - (e / D) * D;
+  // the 8 warps' (m, l, acc) -> this piece's partial for the thread's elements (max-rescale)
+  float o[EPT], L2 = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < EPT; ++i) o[i] = 0.f;
+  if (cm.owns) {
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w)
-      if (ml[w * G + g] > 0.f) M = fmaxf(M, mm[w * G + g]);
-    float num = 0.f, sum = 0.f;
+      if (ml[w * G + cm.g] > 0.f) M = fmaxf(M, mm[w * G + cm.g]);
+    float num[EPT], sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < EPT; ++i) num[i] = 0.f;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) {
-      const float l = ml[w * G + g];
-      if (l > 0.f) {
-        const float f = fast_exp2(mm[w * G + g] - M);
-        sum += f * l;
-        num += f * wbuf[w * W + g * D + d];
+      const float lw = ml[w * G + cm.g];
+      if (lw > 0.f) {
+        const float f = fast_exp2(mm[w * G + cm.g] - M);
+        float a[EPT];
+        load_smem_vec<EPT>(wbuf + w * W + cm.g * D + cm.d0, a);
+        sum += f * lw;
+#pragma unroll
+        for (int i = 0; i < EPT; ++i) num[i] += f * a[i];
       }
     }
-    const float o = sum > 0.f ? num / sum : 0.f;
-    const float L2 = sum > 0.f ? M + fast_log2(sum) : -INFINITY;
-    if (direct) {
-      store_out(p.out, (row0 + g) * D + d, p.out_dtype, o * p.v_scale);
-      if (d == 0) {
-        if (p.out_lse) p.out_lse[row0 + g] = L2 * kLn2;
-        if (p.row_flags && first_phase) p.row_flags[row0 + g] = (uint8_t)((fl >> g) & 1u);
-      }
-    } else {
-      __stcg(p.part_o + ((long long)pc.slot * G + g) * D + d, o);
-      if (d == 0) __stcg(p.part_l + (long long)pc.slot * G + g, L2);
-    }
+#pragma unroll
+    for (int i = 0; i < EPT; ++i) o[i] = sum > 0.f ? num[i] / sum : 0.f;
+    L2 = sum > 0.f ? M + fast_log2(sum) : -INFINITY;
   }
-  if (ctid == 0 && first_phase && fl) {
-    atomicAdd(p.stats + 1, (unsigned long long)__popc(fl));
-    if (direct) {
-      atomicAdd(p.stats + 0, (unsigned long long)__popc(fl));
-      if (p.list_flags) {
-        const int at = atomicAdd(p.list_state, 1);
-        if (at < p.n_groups) p.flag_list[at] = pc.g;
+
+  if (ctid == 0 && first_phase) {
+    if (fl) {
+      atomicAdd(p.stats + 1, (unsigned long long)__popc(fl));
+      if (direct) {
+        atomicAdd(p.stats + 0, (unsigned long long)__popc(fl));
+        if (p.list_flags) {
+          const int at = atomicAdd(p.list_state, 1);
+          if (at < p.n_groups) p.flag_list[at] = pc.g;
+        }
       }
+    }
+    if (p.piece_stats) {
+      const unsigned long long t = (unsigned long long)(pc.t1 - pc.t0);
+      atomicMax(p.stats + 2, t);
+      atomicMax(p.stats + 3, 0x7fffffffull - t);
     }
   }
 
-  if (!direct) {
-    if (ctid == 0) __stcg(p.part_flags + pc.slot, fl);
-    // Arrival: the barrier orders the CTA's partial writes before thread 0's release-acquire
-    // count; the last piece's count also acquires the other pieces' partials.
-    named_bar_sync(1, kCT);
-    if (ctid == 0) {
-      const int old = atom_add_acq_rel_gpu(p.counters + pc.g, 1);
-      misc[0] = old == pc.nslots - 1;
-      misc[1] = 0;
-    }
-    named_bar_sync(1, kCT);
-    if (misc[0]) {
-      // Last piece of the group: merge all its partials. Each thread owns EPT consecutive
-      // elements and issues the loads of up to 64 partial values at once, together with the
-      // LSEs, so a group of up to 64 / EPT pieces pays the L2 latency once.
-      const int S = pc.nslots;
-      float* wts = wbuf;              // [S, G] weights (scratch reused; S <= 8 * D)
-      float* hsum = mm;               // [G] sum of weights
-      float* hmax = ml;               // [G] maximum partial LSE
-      constexpr int EPT = G * D >= 4 * kCT ? 4 : (G * D >= 2 * kCT ? 2 : 1);
-      constexpr int SB = 64 / EPT;
-      const int e0 = ctid * EPT;
-      const bool owner = e0 < G * D;
-      const float* po = p.part_o + (long long)pc.slot_base * G * D + (owner ? e0 : 0);
-      float o[SB][EPT];
-      auto load_block = [&](int s0) {
+  if (direct) {
+    if (cm.owns) {
 #pragma unroll
-        for (int j = 0; j < SB; ++j) {
-          const bool ok = owner && s0 + j < S;
-          const float* src = po + (long long)(s0 + j) * G * D;
-          if constexpr (EPT == 4) {
-            const float4 v = ok ? __ldcg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
-            o[j][0] = v.x;
-            o[j][1] = v.y;
-            o[j][2] = v.z;
-            o[j][3] = v.w;
-          } else if constexpr (EPT == 2) {
-            const float2 v = ok ? __ldcg(reinterpret_cast<const float2*>(src)) : make_float2(0.f, 0.f);
-            o[j][0] = v.x;
-            o[j][1] = v.y;
-          } else {
-            o[j][0] = ok ? __ldcg(src) : 0.f;
-          }
-        }
-      };
-      load_block(0);
-      const float* pl = p.part_l + (long long)pc.slot_base * G;
-      for (int i = ctid; i < S * G; i += kCT) wts[i] = __ldcg(pl + i);
-      uint32_t rf = 0;
-      for (int s = ctid; s < S; s += kCT) rf |= __ldcg(p.part_flags + pc.slot_base + s);
-      rf = __reduce_or_sync(0xffffffffu, rf);
-      if (lane == 0 && rf) atomicOr(reinterpret_cast<unsigned int*>(misc + 1), rf);
-      named_bar_sync(1, kCT);
-      if (warp < G) {
-        const int g = warp;
-        float M = -INFINITY;
-        for (int s = lane; s < S; s += 32) M = fmaxf(M, wts[s * G + g]);
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        float sum = 0.f;
-        for (int s = lane; s < S; s += 32) {
-          const float L = wts[s * G + g];
-          const float f = L > -INFINITY ? fast_exp2(L - M) : 0.f;
-          wts[s * G + g] = f;
-          sum += f;
-        }
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        if (lane == 0) {
-          hsum[g] = sum;
-          hmax[g] = M;
-        }
-      }
-      named_bar_sync(1, kCT);
-      const int g = owner ? e0 / D : 0;   // the thread's EPT elements share one head
-      float num[EPT];
-#pragma unroll
-      for (int i = 0; i < EPT; ++i) num[i] = 0.f;
-      for (int s0 = 0; s0 < S; s0 += SB) {
-        if (s0 > 0) load_block(s0);
-#pragma unroll
-        for (int j = 0; j < SB; ++j) {
-          if (s0 + j < S) {
-            const float w = wts[(s0 + j) * G + g];
-#pragma unroll
-            for (int i = 0; i < EPT; ++i) num[i] += w * o[j][i];
-          }
-        }
-      }
-      const uint32_t rfa = (uint32_t)misc[1];
-      if (owner) {
-        const float sum = hsum[g];
-        const int d0 = e0 - g * D;
-#pragma unroll
-        for (int i = 0; i < EPT; ++i)
-          store_out(p.out, (row0 + g) * D + d0 + i, p.out_dtype,
-                    sum > 0.f ? num[i] / sum * p.v_scale : 0.f);
-        if (d0 == 0) {
-          if (p.out_lse)
-            p.out_lse[row0 + g] = sum > 0.f ? (hmax[g] + fast_log2(sum)) * kLn2 : -INFINITY;
-          if (p.row_flags && first_phase) p.row_flags[row0 + g] = (uint8_t)((rfa >> g) & 1u);
-        }
-      }
-      if (ctid == 0) {
-        p.counters[pc.g] = 0;   // leave the counter ready for the next run
-        if (first_phase && rfa) {
-          atomicAdd(p.stats + 0, (unsigned long long)__popc(rfa));
-          if (p.list_flags) {
-            const int at = atomicAdd(p.list_state, 1);
-            if (at < p.n_groups) p.flag_list[at] = pc.g;
-          }
-        }
+      for (int i = 0; i < EPT; ++i)
+        store_out(p.out, (row0 + cm.g) * D + cm.d0 + i, p.out_dtype, o[i] * p.v_scale);
+      if (cm.d0 == 0) {
+        if (p.out_lse) p.out_lse[row0 + cm.g] = L2 * kLn2;
+        if (p.row_flags && first_phase) p.row_flags[row0 + cm.g] = (uint8_t)((fl >> cm.g) & 1u);
       }
     }
+  } else {
+    merge_last_arriver<T, D, G>(p, pc, first_phase, o, L2, fl, mm, ml, wbuf, misc, warp, lane,
+                                ctid);
   }
   named_bar_sync(1, kCT);   // shared scratch is free for the next piece
 }
@@ -772,8 +840,7 @@ __device__ __forceinline__ void combine_piece(const Params& p, const Piece& pc, 
 template <typename T, int D, int G, bool UNIFIED, bool LOCAL>
 __device__ __forceinline__ void run_consumers(const Params& p, Sched s, uint8_t* stages,
                                               const Layout& L, uint64_t* full, uint64_t* empty,
-                                              uint8_t* smem, int warp, int lane, uint32_t& k,
-                                              bool& dead) {
+                                              uint8_t* smem, int warp, int lane) {
   using C = Cfg<T, D, G>;
   constexpr int E = C::kEpl;
   const uint32_t NS = (uint32_t)p.stages;
@@ -787,6 +854,8 @@ __device__ __forceinline__ void run_consumers(const Params& p, Sched s, uint8_t*
   const int ctid = warp * 32 + lane;
   Piece pc;
   constexpr int E2 = E / 2;
+  uint32_t k = 0;
+  bool dead = false;
   while (sched_next(s, p, pc)) {
     float dl[C::kNv], m[G], mt[G];
     bool sw = false;
@@ -860,7 +929,7 @@ template <typename T, int D, int G, bool UNIFIED, bool LOCAL>
 __device__ __forceinline__ void run_consumers_mma(const Params& p, Sched s, uint8_t* stages,
                                                   const Layout& L, uint64_t* full,
                                                   uint64_t* empty, uint8_t* smem, int warp,
-                                                  int lane, uint32_t& k, bool& dead) {
+                                                  int lane) {
   const uint32_t NS = (uint32_t)p.stages;
   float* wbuf = reinterpret_cast<float*>(smem + L.wbuf_off);
   float* mm = reinterpret_cast<float*>(smem + L.mm_off);
@@ -872,6 +941,8 @@ __device__ __forceinline__ void run_consumers_mma(const Params& p, Sched s, uint
   constexpr bool kFp8 = Cfg<T, D, G>::kFp8;
   const std::conditional_t<kFp8, NoMmaLane, MmaLane<D>> mlane(row0, lane);
   Piece pc;
+  uint32_t k = 0;
+  bool dead = false;
   while (sched_next(s, p, pc)) {
     MmaState<D, G> st;
 #pragma unroll
@@ -956,8 +1027,13 @@ __device__ __forceinline__ Sched launch_sched(const Params& p, const int* lens, 
   s.first_phase = p.recompute == 0;
   if (p.recompute || p.policy != kBalanced) {
     const long long ni = (long long)(p.recompute ? misc[2] : p.n_groups) * s.S;
-    s.i = (long long)blockIdx.x * ni / gridDim.x;
-    s.i1 = ((long long)blockIdx.x + 1) * ni / gridDim.x;
+    if (p.narrow) {
+      s.i = (unsigned)blockIdx.x * (unsigned)ni / gridDim.x;
+      s.i1 = ((unsigned)blockIdx.x + 1u) * (unsigned)ni / gridDim.x;
+    } else {
+      s.i = (long long)blockIdx.x * ni / gridDim.x;
+      s.i1 = ((long long)blockIdx.x + 1) * ni / gridDim.x;
+    }
   } else {
     s.W = (long long)p.hkv * prefix[p.batch];
     // The grid is sized from the cache capacity; when the step holds fewer units than CTAs,
@@ -965,8 +1041,13 @@ __device__ __forceinline__ Sched launch_sched(const Params& p, const int* lens, 
     // pieces sit on consecutive CTAs (its piece count is then cl - cf + 1).
     s.P = (int)(s.W < (long long)gridDim.x ? s.W : (long long)gridDim.x);
     if ((int)blockIdx.x < s.P) {
-      s.u = (long long)blockIdx.x * s.W / s.P;
-      s.u1 = ((long long)blockIdx.x + 1) * s.W / s.P;
+      if (p.narrow) {
+        s.u = (unsigned)blockIdx.x * (unsigned)s.W / (unsigned)s.P;
+        s.u1 = ((unsigned)blockIdx.x + 1u) * (unsigned)s.W / (unsigned)s.P;
+      } else {
+        s.u = (long long)blockIdx.x * s.W / s.P;
+        s.u1 = ((long long)blockIdx.x + 1) * s.W / s.P;
+      }
     }
   }
   return s;
@@ -985,14 +1066,10 @@ __device__ __forceinline__ void consumer_role(const Params& p, int warp, int lan
   const Sched s = launch_sched(p, reinterpret_cast<const int*>(smem + L.lens_off),
                                reinterpret_cast<const int*>(smem + L.prefix_off),
                                reinterpret_cast<const int*>(smem + L.misc_off));
-  uint32_t k = 0;
-  bool dead = false;
   if constexpr (kMma)
-    run_consumers_mma<T, D, G, UNIFIED, LOCAL>(p, s, smem, L, full, empty, smem, warp, lane, k,
-                                               dead);
+    run_consumers_mma<T, D, G, UNIFIED, LOCAL>(p, s, smem, L, full, empty, smem, warp, lane);
   else
-    run_consumers<T, D, G, UNIFIED, LOCAL>(p, s, smem, L, full, empty, smem, warp, lane, k,
-                                           dead);
+    run_consumers<T, D, G, UNIFIED, LOCAL>(p, s, smem, L, full, empty, smem, warp, lane);
 }
 
 // A producer-warpgroup warp's role (two warps issue copies for a contiguous cache, four for a
@@ -1011,10 +1088,7 @@ __device__ __forceinline__ void producer_role(const Params& p, const CUtensorMap
   const Sched s = launch_sched(p, reinterpret_cast<const int*>(smem + L.lens_off),
                                reinterpret_cast<const int*>(smem + L.prefix_off),
                                reinterpret_cast<const int*>(smem + L.misc_off));
-  uint32_t k = 0;
-  bool dead = false;
-  run_producer<T, D, G, k4d>(p, s, smem, L, full, empty, tmk, tmv, lane, warp - kConsumerWarps,
-                              k, dead);
+  run_producer<T, D, G, k4d>(p, s, smem, L, full, empty, tmk, tmv, lane, warp - kConsumerWarps);
 }
 
 // The split kernel. A step's first launch computes every group with the step's softmax mode
@@ -1057,31 +1131,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&tmv);
     }
     if (!p.recompute && p.policy == kBalanced) {
-      for (int b = tid; b < p.batch; b += blockDim.x) {
-        const int raw = __ldg(p.seq_lens + b);
-        const int n = clamp_len(p, raw);
-        if (n != raw && blockIdx.x == 0) atomicOr(p.status, kStatusBadSeqLen);
-        lens[b] = n;
-      }
-      __syncthreads();
-      if (warp == 0) {
-        const int per = (p.batch + 31) / 32;
-        const int beg = min(p.batch, lane * per), end = min(p.batch, beg + per);
-        int local = 0;
-        for (int b = beg; b < end; ++b)
-          local += lens[b] ? (lens[b] + p.unit - 1) / p.unit + p.piece_units : 0;
-        int incl = local;
+      if (p.batch <= 32) {
+        // One warp (not thread 0, which initialises the barriers meanwhile) loads the lengths
+        // and builds the unit prefix with shuffles: one CTA barrier in the whole prologue.
+        if (warp == 1) {
+          int n = 0;
+          if (lane < p.batch) {
+            const int raw = __ldg(p.seq_lens + lane);
+            n = clamp_len(p, raw);
+            if (n != raw && blockIdx.x == 0) atomicOr(p.status, kStatusBadSeqLen);
+            lens[lane] = n;
+          }
+          const int units = n ? (n + p.unit - 1) / p.unit + p.piece_units : 0;
+          int incl = units;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
+          for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+          }
+          if (lane < p.batch) prefix[lane] = incl - units;
+          if (lane == p.batch - 1) prefix[p.batch] = incl;
         }
-        int run = incl - local;
-        for (int b = beg; b < end; ++b) {
-          prefix[b] = run;
-          run += lens[b] ? (lens[b] + p.unit - 1) / p.unit + p.piece_units : 0;
+        __syncthreads();
+      } else {
+        for (int b = tid; b < p.batch; b += blockDim.x) {
+          const int raw = __ldg(p.seq_lens + b);
+          const int n = clamp_len(p, raw);
+          if (n != raw && blockIdx.x == 0) atomicOr(p.status, kStatusBadSeqLen);
+          lens[b] = n;
         }
-        if (lane == 31) prefix[p.batch] = incl;
+        __syncthreads();
+        if (warp == 0) {
+          const int per = (p.batch + 31) / 32;
+          const int beg = min(p.batch, lane * per), end = min(p.batch, beg + per);
+          int local = 0;
+          for (int b = beg; b < end; ++b)
+            local += lens[b] ? (lens[b] + p.unit - 1) / p.unit + p.piece_units : 0;
+          int incl = local;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+          }
+          int run = incl - local;
+          for (int b = beg; b < end; ++b) {
+            prefix[b] = run;
+            run += lens[b] ? (lens[b] + p.unit - 1) / p.unit + p.piece_units : 0;
+          }
+          if (lane == 31) prefix[p.batch] = incl;
+        }
+        __syncthreads();
       }
       // sequences with no tokens have no piece: out = 0, lse = -inf, flag = 0
       for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
@@ -1094,8 +1193,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (p.row_flags) p.row_flags[r0 + h] = 0;
         }
       }
+    } else {
+      __syncthreads();   // the barriers are initialised
     }
-    __syncthreads();
   }
   // a dependent launch (the recompute) may start its launch while this grid runs
   if (!p.recompute) pdl_launch_dependents();

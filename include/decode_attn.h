@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define DECODE_ATTN_ABI_VERSION 2
+#define DECODE_ATTN_ABI_VERSION 3
 
 /* Largest bin count decode_attn_logit_histogram accepts. */
 #define DECODE_ATTN_MAX_HIST_BINS 32768
@@ -135,6 +135,10 @@ typedef struct {
   int max_splits;           /* largest num_splits a run may ask for with this workspace */
   size_t workspace_bytes;   /* device workspace the runs need */
   size_t smem_bytes;        /* dynamic shared memory per CTA */
+  int split_tokens;         /* largest split (piece of one sequence's KV head, in tokens) of a
+                               step whose sequences are all at capacity, under the plan's
+                               default policy ("the split size" of Flash-Decoding) */
+  int split_tokens_min;     /* smallest such split */
 } da_plan_info;
 
 /* Filled by decode_attn_run when requested (forces a stream synchronisation). */
@@ -144,6 +148,9 @@ typedef struct {
   long long rows_flagged;   /* UNIFIED: (b, h) rows whose range check failed */
   long long splits_flagged; /* UNIFIED: (split, h) partials whose range check failed */
   int recompute_launched;   /* 1 iff the recompute kernel was enqueued (DA_SOFTMAX_UNIFIED) */
+  int split_tokens;         /* largest split of this run's first pass, in tokens (the split
+                               the heuristic chose, as the device cut it from seq_lens) */
+  int split_tokens_min;     /* smallest split of this run's first pass, in tokens */
 } da_stats;
 
 /* Validate a problem and choose the launch (grid, split policy, pipeline) for it.
@@ -161,8 +168,10 @@ int decode_attn_plan(const da_problem* problem, int num_splits, da_plan** plan_o
 /* Copy what the plan chose into *info. Errors: INVALID_ARG. */
 int decode_attn_plan_info(const da_plan* plan, da_plan_info* info);
 
-/* Zero the workspace's self-cleaning counters. Required once for a new workspace before
- * its first run (a zero-filled allocation needs no call). Enqueued on `stream`.
+/* Zero the part of the workspace that runs expect at zero and leave at zero (counters and the
+ * flagged list). Required once for a new workspace before its first run (a zero-filled
+ * allocation needs no call), and again after a run reported DA_ERR_DEVICE_TIMEOUT. Enqueued
+ * on `stream`.
  * Errors: INVALID_ARG, WORKSPACE_TOO_SMALL, CUDA. */
 int decode_attn_workspace_init(const da_plan* plan, void* workspace, size_t workspace_bytes,
                                void* cuda_stream);
@@ -244,19 +253,25 @@ int decode_attn_run_ex(const da_plan* plan, const da_run_args* args);
  * loaded on the device. The call itself allocates nothing: no cudaMalloc, no cudaFree, no
  * allocating library routine.
  *   Arguments as for decode_attn_run, less workspace and workspace_bytes.
- *   First call on a device: it looks up the region's device address (with that device
- *   current, as every call must have) and caches it, which can load the library's device
- *   code on that device. Make the first call on each device before any stream capture.
- *   Each call clears the region's counters on `cuda_stream` before the run, so runs of
- *   different plans may follow one another on a stream.
+ *   First call in a CUDA context: it looks up the region's device address in the context
+ *   current on the calling thread (which can load the library's device code there) and
+ *   caches it under that context's unique ID; a device reset or a caller's own driver
+ *   context therefore gets a lookup of its own. Make the first call in each context before
+ *   any stream capture.
+ *   Each call first clears, on `cuda_stream`, the part of the region the plan's run expects
+ *   at zero (counters and the flagged list), so runs of different plans may follow one another
+ *   on a stream.
  *   Overlapping calls race: all calls on one device share the one region, so two calls
  *   whose work can overlap on the GPU (other streams, other host threads, other plans)
  *   corrupt each other's results. Serialise them, or use decode_attn_run with separate
  *   workspaces.
+ *   Device findings (bad block-table entries or lengths, pipeline timeouts) are reported
+ *   only through `stats` or the problem's `validate` flag: the region's status word is
+ *   cleared by the next call.
  * Errors: as decode_attn_run; WORKSPACE_TOO_SMALL also when the plan's workspace_bytes
  * exceeds DECODE_ATTN_STATIC_SCRATCH_BYTES (use decode_attn_run with a workspace of that
- * size instead); UNSUPPORTED on a device with ordinal 64 or above. Argument errors are
- * detected before anything is enqueued. */
+ * size instead). Argument errors, including a plan whose kernel is not built, are detected
+ * before anything is enqueued. */
 int decode_attn_run_static(const da_plan* plan, const void* q, const void* k_cache,
                            const void* v_cache, const int32_t* block_table,
                            const int32_t* seq_lens, float scale, int num_splits, void* out,

@@ -35,7 +35,7 @@ def test_library_exports_every_header_symbol(L):
 
 
 def test_abi_version_and_strerror(L):
-    assert binding.decode_attn_abi_version() == 2
+    assert binding.decode_attn_abi_version() == 3
     for code in binding.ERRORS:
         assert binding.decode_attn_strerror(code)
     assert "unknown" in binding.decode_attn_strerror(-99)
@@ -148,6 +148,26 @@ def test_workspace_holds_the_split_partials(L):
     part_o = 1 * 32 * 128 * 128 * 2 * 2
     assert part_o == 2 * 1048576
     assert part_o <= ws <= part_o + 96 * 1024
+    binding.decode_attn_destroy(plan)
+
+
+def test_plan_reports_the_split_size(L):
+    # 32K GQA on 152 SMs: 8 groups of 32768 tokens over 152 balanced shares, 19 per group, so
+    # every split holds about 32768 / 19 tokens, in whole 16-token units
+    plan, _ = binding.decode_attn_plan(_prob(max_seq_len=32768), 0)
+    info = binding.decode_attn_plan_info(plan)
+    assert info.num_splits == 0 and info.grid_ctas == 152
+    assert info.split_tokens % 16 == 0 and info.split_tokens_min % 16 == 0
+    assert 32768 // 19 - 16 * 13 <= info.split_tokens_min <= info.split_tokens <= 32768 // 19 + 32
+    binding.decode_attn_destroy(plan)
+    # uniform splits: roundup(ceil(4096 / 16), 16) = 256 tokens each
+    plan, _ = binding.decode_attn_plan(_prob(num_kv_heads=32, max_seq_len=4096), 16)
+    info = binding.decode_attn_plan_info(plan)
+    assert (info.split_tokens, info.split_tokens_min) == (256, 256)
+    binding.decode_attn_destroy(plan)
+    plan, _ = binding.decode_attn_plan(_prob(max_seq_len=1000), 3)
+    info = binding.decode_attn_plan_info(plan)
+    assert (info.split_tokens, info.split_tokens_min) == (336, 328)
     binding.decode_attn_destroy(plan)
 
 
