@@ -55,6 +55,7 @@ class da_problem(ctypes.Structure):
         ("kv_fp8", ctypes.c_int),
         ("k_scale", ctypes.c_float),
         ("v_scale", ctypes.c_float),
+        ("debug_stall_stage", ctypes.c_int),
     ]
 
 
@@ -279,7 +280,8 @@ def decode_attn_destroy(plan):
 def make_problem(*, batch, num_q_heads, num_kv_heads, head_dim, qkv_dtype, out_dtype, paged=False,
                  page_size=16, max_blocks_per_seq=0, num_physical_blocks=0, max_seq_len=0,
                  mode="sync", unified_max=0.0, range_lo=-64.0, range_hi=64.0, validate=False,
-                 num_sms=0, kv_dtype=None, k_scale=1.0, v_scale=1.0) -> da_problem:
+                 num_sms=0, kv_dtype=None, k_scale=1.0, v_scale=1.0,
+                 debug_stall_stage=0) -> da_problem:
     """kv_dtype=None: K / V stored as qkv_dtype; "e4m3": an FP8 cache of codes standing for
     code * k_scale and code * v_scale (q stays qkv_dtype, which must be bf16)."""
     if kv_dtype not in (None, qkv_dtype, "e4m3"):
@@ -289,7 +291,7 @@ def make_problem(*, batch, num_q_heads, num_kv_heads, head_dim, qkv_dtype, out_d
                       max_blocks_per_seq, num_physical_blocks, max_seq_len,
                       DTYPE_CODES[qkv_dtype], DTYPE_CODES[out_dtype], MODE_CODES[mode],
                       unified_max, range_lo, range_hi, int(bool(validate)), num_sms, int(fp8),
-                      k_scale if fp8 else 1.0, v_scale if fp8 else 1.0)
+                      k_scale if fp8 else 1.0, v_scale if fp8 else 1.0, int(debug_stall_stage))
 
 
 # ---- torch-facing convenience (marshalling only) -------------------------------------------

@@ -288,6 +288,7 @@ int validate_problem(const da_problem& p) {
     if ((long long)p.batch * p.max_seq_len >= (1ll << 31)) return DA_ERR_INVALID_ARG;
   }
   if (p.kv_fp8 != 0 && p.kv_fp8 != 1) return DA_ERR_INVALID_ARG;
+  if (p.debug_stall_stage < 0) return DA_ERR_INVALID_ARG;
   if (p.kv_fp8) {
     // FP8 caches run on the tensor-core consumers: bf16 q, groups of 4 or 8 heads
     if (p.qkv_dtype != DA_BF16 || (G != 4 && G != 8)) return DA_ERR_UNSUPPORTED;
@@ -447,6 +448,8 @@ void fill_common(const da_plan& pl, Params& k, const int32_t* block_table,
   k.stages = pl.stages;
   k.batch_smem = pl.batch_smem;
   k.narrow = pl.narrow;
+  k.stall_stage = p.debug_stall_stage;
+  k.wait_limit_ns = p.debug_stall_stage ? kTestWaitLimitNs : kWaitLimitNs;
 }
 
 int status_to_error(int s) {

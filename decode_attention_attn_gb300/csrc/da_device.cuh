@@ -39,6 +39,8 @@ constexpr int kStatusTimeout = 4;
 
 // bound on any pipeline wait (ns); a healthy wait lasts microseconds
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+// the bound while the test hook that stalls a stage is on
+constexpr unsigned long long kTestWaitLimitNs = 2000000ull;
 
 enum Policy { kBalanced = 0, kUniform = 1 };
 // Softmax modes, numbered as the C ABI's da_softmax_mode.
@@ -89,6 +91,9 @@ struct Params {
   int recompute;                 // 1: the recompute launch (groups from the flagged list)
   int list_flags;                // 1: flagged groups go to the list (a recompute launch follows)
   int piece_stats;               // 1: record the largest and smallest piece in stats[2..3]
+  unsigned long long wait_limit_ns;   // bound on every pipeline wait
+  int stall_stage;               // test hook: 0, or k + 1: CTA 0's producer neither arms nor
+                                 // fills ring stage k, so that its consumers' wait runs out
   int narrow;                    // 1: every product of the schedule's unit / item arithmetic
                                  // (index x CTA count) is below 2^31: 32-bit division suffices
   int n_groups;                  // B * Hkv
@@ -215,16 +220,17 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
   return t;
 }
 
-// Wait for the phase of `parity` to complete, for at most kWaitLimitNs. Returns false on
+// Wait for the phase of `parity` to complete, for at most `limit_ns`. Returns false on
 // timeout (the caller records it and degrades to a non-waiting completion).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 

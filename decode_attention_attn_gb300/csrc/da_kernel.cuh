@@ -165,11 +165,14 @@ __device__ __forceinline__ bool sched_next(Sched& s, const Params& p, Piece& pc)
 // Copies are issued by two warps (part 0: K and q, part 1: V) for a contiguous cache and by
 // four for a paged one (parts 2 and 3 take every other page box): one warp's TMA issue rate
 // cannot keep up with a stage made of several small page boxes.
+// `abort`: set by a consumer warp whose wait ran out; the producer then issues nothing more (a
+// stage the consumers released without waiting for it may still have copies in flight into its
+// slot) and leaves after draining the copies it issued.
 template <typename T, int D, int G, bool SWZ>
 __device__ __forceinline__ void run_producer(const Params& p, Sched s, uint8_t* stages,
                                              const Layout& L, uint64_t* full, uint64_t* empty,
                                              const CUtensorMap* tmk, const CUtensorMap* tmv,
-                                             int lane, int part) {
+                                             int lane, int part, const int* abort) {
   using C = Cfg<T, D, G>;
   const uint64_t pol = make_evict_first_policy();
   const uint32_t NS = (uint32_t)p.stages;
@@ -189,12 +192,16 @@ __device__ __forceinline__ void run_producer(const Params& p, Sched s, uint8_t* 
     int32_t win = -1, wnext = -1;
     for (int ts = pc.t0, j = 0; ts < pc.t1; ts += kStageTokens, ++j, ++k) {
       const uint32_t slot = k % NS, ph = (k / NS) & 1u;
-      if (!dead && !mbar_wait(&empty[slot], ph ^ 1u)) {
+      if (!dead && !mbar_wait(&empty[slot], ph ^ 1u, p.wait_limit_ns)) {
         dead = true;
         if (lane == 0) atomicOr(p.status, kStatusTimeout);
       }
+      if (!dead && *reinterpret_cast<const volatile int*>(abort) != 0) dead = true;
       dead = __any_sync(0xffffffffu, dead);   // several lanes issue copies: agree on it
       if (!dead) issued = k + 1;
+      // test hook: this stage is neither armed nor filled
+      const bool skip = dead || (p.stall_stage != 0 && blockIdx.x == 0 &&
+                                 k == (uint32_t)(p.stall_stage - 1));
       const int n = min(kStageTokens, pc.t1 - ts);
       uint8_t* st = stages + slot * L.stage_bytes;
       if (p.paged) {
@@ -226,14 +233,14 @@ __device__ __forceinline__ void run_producer(const Params& p, Sched s, uint8_t* 
           if (bi < nbox) atomicOr(p.status, kStatusBadBlockTable);
           z = p.num_blocks * p.page_size;   // past the pool: the box reads as zeros
         }
-        if (part == 0 && lane == 0 && !dead) {
+        if (part == 0 && lane == 0 && !skip) {
           const uint32_t bytes =
               (uint32_t)nbox * box * C::kRowBytes * 2u + (j == 0 ? (uint32_t)C::kQBytes : 0u);
           mbar_arrive_expect_tx(&full[slot], bytes);
           if (j == 0) bulk_load(st + L.q_off, qsrc, C::kQBytes, &full[slot]);
         }
         __syncwarp();
-        if (bi < nbox && !dead) {
+        if (bi < nbox && !skip) {
           const uint32_t off = ((part & 1) == 0 ? L.k_off : L.v_off) + bi * box * C::kRowBytes;
           const CUtensorMap* tm = (part & 1) == 0 ? tmk : tmv;
           if constexpr (SWZ)
@@ -241,7 +248,7 @@ __device__ __forceinline__ void run_producer(const Params& p, Sched s, uint8_t* 
           else
             tma_load_3d(st + off, tm, &full[slot], 0, pc.kvh, z, pol);
         }
-      } else if (lane == 0 && !dead) {
+      } else if (lane == 0 && !skip) {
         const int z = pc.b * p.max_seq_len + ts;
         if (part == 0) {
           const uint32_t bytes =
@@ -263,7 +270,8 @@ __device__ __forceinline__ void run_producer(const Params& p, Sched s, uint8_t* 
   // after a timeout too.
   if (lane == 0) {
     const uint32_t first = issued > NS ? issued - NS : 0u;
-    for (uint32_t kk = first; kk < issued; ++kk) mbar_wait(&full[kk % NS], (kk / NS) & 1u);
+    for (uint32_t kk = first; kk < issued; ++kk)
+      mbar_wait(&full[kk % NS], (kk / NS) & 1u, p.wait_limit_ns);
   }
 }
 
@@ -670,7 +678,7 @@ __device__ __forceinline__ void merge_last_arriver(const Params& p, const Piece&
   float* wts = wbuf;              // [S, G] weights (scratch reused; S <= 8 * D)
   float* hsum = mm;               // [G] sum of weights
   float* hmax = ml;               // [G] maximum partial LSE
-  constexpr int SB = 64 / EPT;
+  constexpr int SB = 16;   // partials per round of loads (a small block keeps this rarely run code short)
   const float* po = p.part_o + (long long)pc.slot_base * G * D + (cm.owns ? cm.e0 : 0);
   float ob[SB][EPT];
   auto load_block = [&](int s0) {
@@ -855,7 +863,7 @@ __device__ __forceinline__ void run_consumers(const Params& p, Sched s, uint8_t*
   Piece pc;
   constexpr int E2 = E / 2;
   uint32_t k = 0;
-  bool dead = false;
+  bool dead = false, gave_up = false;
   while (sched_next(s, p, pc)) {
     float dl[C::kNv], m[G], mt[G];
     bool sw = false;
@@ -877,13 +885,13 @@ __device__ __forceinline__ void run_consumers(const Params& p, Sched s, uint8_t*
     for (int j = 0; j < nst; j += 2) {
       const bool pair = j + 1 < nst;
       const uint32_t s0 = k % NS, s1 = (k + 1) % NS;
-      if (!dead && !mbar_wait(&full[s0], (k / NS) & 1u)) {
+      if (!dead && !mbar_wait(&full[s0], (k / NS) & 1u, p.wait_limit_ns)) dead = true;
+      if (pair && !dead && !mbar_wait(&full[s1], ((k + 1) / NS) & 1u, p.wait_limit_ns))
         dead = true;
-        if (lane == 0) atomicOr(p.status, kStatusTimeout);
-      }
-      if (pair && !dead && !mbar_wait(&full[s1], ((k + 1) / NS) & 1u)) {
-        dead = true;
-        if (lane == 0) atomicOr(p.status, kStatusTimeout);
+      if (dead && lane == 0 && !gave_up) {
+        gave_up = true;
+        atomicOr(p.status, kStatusTimeout);
+        atomicExch(misc + 3, 1);   // the producer stops issuing
       }
       const uint8_t* st0 = stages + s0 * L.stage_bytes;
       const uint8_t* st1 = stages + s1 * L.stage_bytes;
@@ -942,7 +950,7 @@ __device__ __forceinline__ void run_consumers_mma(const Params& p, Sched s, uint
   const std::conditional_t<kFp8, NoMmaLane, MmaLane<D>> mlane(row0, lane);
   Piece pc;
   uint32_t k = 0;
-  bool dead = false;
+  bool dead = false, gave_up = false;
   while (sched_next(s, p, pc)) {
     MmaState<D, G> st;
 #pragma unroll
@@ -959,13 +967,13 @@ __device__ __forceinline__ void run_consumers_mma(const Params& p, Sched s, uint
     for (int j = 0; j < nst; j += 2) {
       const bool pair = j + 1 < nst;
       const uint32_t s0 = k % NS, s1 = (k + 1) % NS;
-      if (!dead && !mbar_wait(&full[s0], (k / NS) & 1u)) {
+      if (!dead && !mbar_wait(&full[s0], (k / NS) & 1u, p.wait_limit_ns)) dead = true;
+      if (pair && !dead && !mbar_wait(&full[s1], ((k + 1) / NS) & 1u, p.wait_limit_ns))
         dead = true;
-        if (lane == 0) atomicOr(p.status, kStatusTimeout);
-      }
-      if (pair && !dead && !mbar_wait(&full[s1], ((k + 1) / NS) & 1u)) {
-        dead = true;
-        if (lane == 0) atomicOr(p.status, kStatusTimeout);
+      if (dead && lane == 0 && !gave_up) {
+        gave_up = true;
+        atomicOr(p.status, kStatusTimeout);
+        atomicExch(misc + 3, 1);   // the producer stops issuing
       }
       const uint8_t* st0 = stages + s0 * L.stage_bytes;
       const uint8_t* st1 = stages + s1 * L.stage_bytes;
@@ -1088,7 +1096,8 @@ __device__ __forceinline__ void producer_role(const Params& p, const CUtensorMap
   const Sched s = launch_sched(p, reinterpret_cast<const int*>(smem + L.lens_off),
                                reinterpret_cast<const int*>(smem + L.prefix_off),
                                reinterpret_cast<const int*>(smem + L.misc_off));
-  run_producer<T, D, G, k4d>(p, s, smem, L, full, empty, tmk, tmv, lane, warp - kConsumerWarps);
+  run_producer<T, D, G, k4d>(p, s, smem, L, full, empty, tmk, tmv, lane, warp - kConsumerWarps,
+                              reinterpret_cast<const int*>(smem + L.misc_off) + 3);
 }
 
 // The split kernel. A step's first launch computes every group with the step's softmax mode
@@ -1125,6 +1134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_mbar_init();
       if (p.recompute) misc[2] = min(__ldcg(p.list_state), p.n_groups);
+      misc[3] = 0;   // set when a consumer's wait runs out
     }
     if (warp == kConsumerWarps && lane == 0) {
       prefetch_tensormap(&tmk);

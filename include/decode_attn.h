@@ -119,6 +119,13 @@ typedef struct {
   int kv_fp8;
   float k_scale;
   float v_scale;
+  /* Test hook, 0 in normal use. k > 0: in every run of the plan, CTA 0's copy producer neither
+   * arms nor fills ring stage k - 1 (no copy is issued for it) and every pipeline wait gives up
+   * after 2 ms instead of 2 s, so that the consumers waiting for that stage run out of time:
+   * the device records DA_ERR_DEVICE_TIMEOUT, the producer issues nothing more and drains the
+   * copies it issued, and the run ends with unspecified outputs (with validate set, the call
+   * returns DA_ERR_DEVICE_TIMEOUT). This exercises the bounded-wait path without a fault. */
+  int debug_stall_stage;
 } da_problem;
 
 typedef struct da_plan da_plan;   /* opaque, host-owned, immutable after creation */

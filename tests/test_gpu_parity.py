@@ -318,6 +318,39 @@ def test_bad_block_table_is_reported_not_read():
     _parity.compare(out[0], ref.reshape(out[0].shape), "bf16", where="bad table, clean seq")
 
 
+def test_pipeline_timeout_is_reported_and_cleared():
+    """The bounded-wait path, without a fault: a test hook makes CTA 0's producer leave its
+    first ring stage unarmed and unfilled and shortens every wait to 2 ms, so its consumers'
+    wait runs out. The run reports DA_ERR_DEVICE_TIMEOUT (validate), the status word of a run
+    without validate reads once and is cleared by decode_attn_check_status, and the same
+    workspace then serves an ordinary run exactly."""
+    wl = workloads.GQA_32K.replace(name="timeout", seq_len=4096)
+    inp = workloads.generate(wl)
+    dev = _parity.DeviceInputs(inp)
+    prob = _parity.problem_for(inp, validate=True)
+    prob.debug_stall_stage = 1
+    with pytest.raises(binding.DecodeAttnError) as e:
+        binding.DecodeAttention(prob, 0).run(dev.q, dev.k, dev.v, dev.bt, dev.sl, wl.scale)
+    assert e.value.code == -6   # DA_ERR_DEVICE_TIMEOUT
+    prob = _parity.problem_for(inp)
+    prob.debug_stall_stage = 1
+    stalled = binding.DecodeAttention(prob, 0)
+    stalled.run(dev.q, dev.k, dev.v, dev.bt, dev.sl, wl.scale)
+    stream = torch.cuda.current_stream().cuda_stream
+    with pytest.raises(binding.DecodeAttnError) as e:
+        binding.decode_attn_check_status(stalled.plan, stalled.workspace.data_ptr(), stream)
+    assert e.value.code == -6
+    binding.decode_attn_check_status(stalled.plan, stalled.workspace.data_ptr(), stream)
+    plain = binding.DecodeAttention(_parity.problem_for(inp), 0)
+    assert plain.workspace_bytes == stalled.workspace_bytes
+    plain.workspace = stalled.workspace   # the workspace the timed-out runs used
+    out, lse, _ = plain.run(dev.q, dev.k, dev.v, dev.bt, dev.sl, wl.scale)
+    torch.cuda.synchronize()
+    ref, ref_lse, _, _ = _parity.run_oracle(inp)
+    _parity.compare(out, ref.reshape(out.shape), wl.out_dtype, where="after a timeout")
+    _parity.compare_lse(lse, ref_lse.reshape(lse.shape), where="after a timeout")
+
+
 def test_bad_seq_len_is_reported():
     wl = workloads.GQA_32K.replace(name="badlen", batch=2, seq_len=256)
     inp = workloads.generate(wl)
