@@ -285,16 +285,21 @@ def launches_per_step(mode):
 # Workloads measured beside the headline by the default run: the other named configurations
 # of the gate and the stress test's fallback rates (paged batch, Llama2-7B-shaped MHA, the
 # unified-max stress in both unified modes), plus the FP8 caches.
-SIDE_WORKLOADS = [("mha", "unified_local"), ("paged", "unified_local"), ("stress", "unified"),
-                  ("stress", "unified_local"), ("gqa32k_fp8", "unified_local"),
-                  ("paged_fp8", "unified_local")]
+# (workload, softmax mode, split override): the MHA step runs with its stated 16 splits of
+# 256 tokens and once more with the library's balanced shares (None: the workload's own).
+SIDE_WORKLOADS = [("mha", "unified_local", None), ("mha", "unified_local", 0),
+                  ("paged", "unified_local", None), ("stress", "unified", None),
+                  ("stress", "unified_local", None), ("gqa32k_fp8", "unified_local", None),
+                  ("paged_fp8", "unified_local", None)]
 
 
-def measure_side(name, mode, args, dev_name, stream, flush, peak, peak_kind):
+def measure_side(name, mode, splits, args, dev_name, stream, flush, peak, peak_kind):
     """One side workload: step and split-kernel time spread, GB/s, roofline and fallback rates."""
     import torch
     from decode_attention_attn_gb300 import binding, harness, workloads
     wl = workloads.get(name).replace(mode=mode)
+    if splits is not None:
+        wl = wl.replace(num_splits=splits)
     inp = workloads.generate(wl)
     kv_bytes = inp.kv_bytes()
     dev = harness.DeviceInputs(inp, dev_name)
@@ -310,6 +315,8 @@ def measure_side(name, mode, args, dev_name, stream, flush, peak, peak_kind):
     ms = statistics.median(step_ms)
     km = statistics.median(kern_ms)
     res = {"workload": wl.name, "softmax": mode, "kv_dtype": wl.kv_storage,
+           "splits": (f"{wl.num_splits} uniform splits" if wl.num_splits > 0
+                      else "heuristic (balanced shares)"),
            "kv_bytes_per_step": kv_bytes, "us_per_step": spread(step_ms),
            "value": round(kv_bytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
            "pct_hbm_peak": round(100 * kv_bytes / (ms * 1e-3) / 1e9 / peak, 2),
@@ -318,7 +325,7 @@ def measure_side(name, mode, args, dev_name, stream, flush, peak, peak_kind):
                         "frac": round(kv_bytes / (km * 1e-3) / 1e9 / peak, 4),
                         "peak_source": f"{peak_kind} hbm_gbs", "kernel": "decode_split_kernel",
                         "kernel_us": spread(kern_ms),
-                        "traffic": profiled_traffic(wl.name)},
+                        "traffic": profiled_traffic(wl.name) if splits is None else None},
            "clocks": clocks, "steps": steps, "gpu_launches": launches_per_step(mode) * steps,
            "grid_ctas": attn.info.grid_ctas,
            "split_tokens": [stats.split_tokens_min, stats.split_tokens]}
@@ -347,7 +354,8 @@ def run_ours(args):
     inp = workloads.generate(wl, offset=rank)
     kv_bytes = inp.kv_bytes()
     dev = harness.DeviceInputs(inp, dev_name)
-    plan_splits = 0 if args.num_splits < 0 else args.num_splits
+    # the workload's own split choice (uniform splits for the MHA step) unless --num-splits
+    plan_splits = wl.num_splits if args.num_splits < 0 else args.num_splits
     attn = binding.DecodeAttention(harness.problem_for(inp, mode=args.mode), plan_splits)
     stream = torch.cuda.current_stream()
     flush = L2Flush(dev_name)
@@ -412,8 +420,8 @@ def run_ours(args):
     side = []
     if rank == 0 and world == 1 and not args.no_side and args.workload == "gqa32k" \
             and args.num_splits < 0:
-        side = [measure_side(n, m, args, dev_name, stream, flush, peak, peak_kind)
-                for n, m in SIDE_WORKLOADS]
+        side = [measure_side(n, m, sp, args, dev_name, stream, flush, peak, peak_kind)
+                for n, m, sp in SIDE_WORKLOADS]
 
     if world > 1:
         dist.barrier()
@@ -443,7 +451,9 @@ def run_ours(args):
                    "kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
                    "kv_tokens_per_seq": int(inp.seq_lens.max()), "kv_dtype": wl.kv_storage,
                    "out_dtype": wl.out_dtype, "softmax": args.mode,
-                   "splits": "heuristic (balanced shares)" if args.num_splits < 0 else args.num_splits,
+                   "splits": (args.num_splits if args.num_splits >= 0 else
+                              (f"{wl.num_splits} uniform splits" if wl.num_splits > 0
+                               else "heuristic (balanced shares)")),
                    "grid_ctas": attn.info.grid_ctas, "stages": attn.info.stages,
                    "split_tokens": [stats.split_tokens_min, stats.split_tokens],
                    "kv_bytes_per_step": kv_bytes,

@@ -290,8 +290,8 @@ int validate_problem(const da_problem& p) {
   if (p.kv_fp8 != 0 && p.kv_fp8 != 1) return DA_ERR_INVALID_ARG;
   if (p.debug_stall_stage < 0) return DA_ERR_INVALID_ARG;
   if (p.kv_fp8) {
-    // FP8 caches run on the tensor-core consumers: bf16 q, groups of 4 or 8 heads
-    if (p.qkv_dtype != DA_BF16 || (G != 4 && G != 8)) return DA_ERR_UNSUPPORTED;
+    // FP8 caches run on the tensor-core consumers with bf16 q
+    if (p.qkv_dtype != DA_BF16) return DA_ERR_UNSUPPORTED;
     if (!std::isfinite(p.k_scale) || !std::isfinite(p.v_scale) || !(p.k_scale > 0.f) ||
         !(p.v_scale > 0.f))
       return DA_ERR_INVALID_ARG;
@@ -728,7 +728,7 @@ int decode_attn_run_ex(const da_plan* plan, const da_run_args* args) {
   const bool unified = p.mode == DA_SOFTMAX_UNIFIED;   // the recompute launch follows
 
   // tensor-core kernels (both modes, so the recompute pass too) read 128-byte-swizzled tiles
-  const bool mma = uses_mma(pl.kv_es, p.qkv_dtype == DA_BF16, pl.group);
+  const bool mma = uses_mma(pl.kv_es, p.qkv_dtype == DA_F16, pl.group);
   CUtensorMap tmk, tmv;
   int rc = make_kv_map(pl, k_cache, mma, &tmk);
   if (rc == DA_OK) rc = make_kv_map(pl, v_cache, mma, &tmv);

@@ -114,12 +114,14 @@ struct Layout {
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
 // Split kernels whose consumers run on the tensor cores (see da_mma.cuh), in every softmax
-// mode: bf16 or FP8 caches (es: K / V bytes per element), packed groups of 4 or 8 query
-// heads. bf16 tiles are TMA-loaded with the 128-byte swizzle (4-D view: 64-element rows,
-// d / 64 of them per token, heads, tokens); FP8 tiles as rows of d bytes (3-D view), with the
-// 128-byte swizzle when d = 128.
-__host__ __device__ constexpr bool uses_mma(int es, bool is_bf16, int G) {
-  return (es == 1 || (es == 2 && is_bf16)) && (G == 4 || G == 8);
+// mode: bf16 or FP8 caches (es: K / V bytes per element), groups of 1, 2, 4 or 8 query heads.
+// bf16 tiles are TMA-loaded with the 128-byte swizzle (4-D view: 64-element rows, d / 64 of
+// them per token, heads, tokens); FP8 tiles as rows of d bytes (3-D view), with the 128-byte
+// swizzle when d = 128. f16 caches keep the CUDA-core consumers: with P in f16 the unified
+// phase needs a rescaled P . V per tile, which measured slower than the CUDA-core path on the
+// MHA workload; f32 caches have no 16-bit MMA operand at all.
+__host__ __device__ constexpr bool uses_mma(int es, bool is_f16, int G) {
+  return (es == 1 || (es == 2 && !is_f16)) && (G == 1 || G == 2 || G == 4 || G == 8);
 }
 
 // Geometry of a consumer warp's logit transpose: a KV row of D elements of es bytes is split

@@ -13,8 +13,8 @@
 //               64-row K and V tiles (and, per piece, the group's q) into a ring of
 //               shared-memory stages; paged caches are gathered through the block table one
 //               page per TMA box ("PagedAttention").
-//   warps 0..7  consumers: each takes 8 rows of every stage. For bf16 groups of 4 or 8 heads
-//               the logits and P . V run on the tensor cores (da_mma.cuh). Otherwise a row of
+//   warps 0..7  consumers: each takes 8 rows of every stage. For bf16 and FP8 caches the
+//               logits and P . V run on the tensor cores (da_mma.cuh). Otherwise a row of
 //               d elements is split over a lane group (16 lanes for d = 128 in 16-bit types,
 //               16-byte chunks per lane); q . k partial sums for all heads and rows of the
 //               lane group are completed by a transpose-reduce through shared memory that
@@ -931,8 +931,8 @@ __device__ __forceinline__ void run_consumers(const Params& p, Sched s, uint8_t*
   }
 }
 
-// Tensor-core consumers (unified softmax, bf16, G >= 4): same stage-pair loop as
-// run_consumers, the math in mma_consume.
+// Tensor-core consumers (bf16 or FP8 caches, every softmax mode): same stage-pair loop as
+// run_consumers, the math in mma_consume / mma_consume_fp8.
 template <typename T, int D, int G, bool UNIFIED, bool LOCAL>
 __device__ __forceinline__ void run_consumers_mma(const Params& p, Sched s, uint8_t* stages,
                                                   const Layout& L, uint64_t* full,
@@ -1066,7 +1066,7 @@ template <typename T, int D, int G, int MODE>
 __device__ __forceinline__ void consumer_role(const Params& p, int warp, int lane) {
   constexpr bool UNIFIED = MODE != kSoftmaxSync, LOCAL = MODE == kSoftmaxUnifiedLocal;
   using C = Cfg<T, D, G>;
-  constexpr bool kMma = uses_mma(sizeof(T), std::is_same<T, __nv_bfloat16>::value, G);
+  constexpr bool kMma = uses_mma(sizeof(T), std::is_same<T, __half>::value, G);
   uint8_t* smem = smem_base();
   const Layout L = make_layout(D, G, C::kQEs, p.stages, p.batch_smem, C::kEs);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
@@ -1086,7 +1086,7 @@ template <typename T, int D, int G>
 __device__ __forceinline__ void producer_role(const Params& p, const CUtensorMap* tmk,
                                               const CUtensorMap* tmv, int warp, int lane) {
   using C = Cfg<T, D, G>;
-  constexpr bool kMma = uses_mma(sizeof(T), std::is_same<T, __nv_bfloat16>::value, G);
+  constexpr bool kMma = uses_mma(sizeof(T), std::is_same<T, __half>::value, G);
   constexpr bool k4d = kMma && !C::kFp8;   // bf16 tensor-core tiles: the 4-D swizzled view
   if (warp >= kConsumerWarps + (p.paged ? 4 : 2)) return;
   uint8_t* smem = smem_base();
@@ -1252,17 +1252,5 @@ inline const void* pick_kernel(int G, int mode) {
 #undef DA_CASE
 }
 
-// FP8 caches run on the tensor-core consumers only: groups of 4 or 8 heads.
-template <typename T, int D>
-inline const void* pick_kernel_mma(int G, int mode) {
-  if (G != 4 && G != 8) return nullptr;
-  if (G == 4)
-    return mode == kSoftmaxSync      ? (const void*)&decode_split_kernel<T, D, 4, 0>
-           : mode == kSoftmaxUnified ? (const void*)&decode_split_kernel<T, D, 4, 1>
-                                     : (const void*)&decode_split_kernel<T, D, 4, 2>;
-  return mode == kSoftmaxSync      ? (const void*)&decode_split_kernel<T, D, 8, 0>
-         : mode == kSoftmaxUnified ? (const void*)&decode_split_kernel<T, D, 8, 1>
-                                   : (const void*)&decode_split_kernel<T, D, 8, 2>;
-}
 
 }  // namespace da

@@ -1,16 +1,18 @@
-// da_mma.cuh -- tensor-core consumer for packed GQA groups of G >= 4 query heads over bf16
-// or FP8 (E4M3) caches, in every softmax mode (FP8 tiles: f16 MMAs, see the end of the file).
+// da_mma.cuh -- tensor-core consumer for groups of 1 to 8 query heads over bf16 or FP8
+// (E4M3) caches, in every softmax mode (FP8 tiles: f16 MMAs, see the end of the file).
 //
-// Per KV tile the group's work is two dense contractions (the logits of G heads against the
-// tile's tokens, and P . V). On CUDA cores they made the split kernel issue-bound on GB300
-// (the consumers alone, with no HBM traffic, took about as long as the whole kernel), so for
-// these groups they run on the tensor cores with warp-level m16n8k16 bf16 MMAs, in transposed
-// form so that the 16 rows of the MMA are never wasted on a small group:
+// Per KV tile the group's work is two contractions (the logits of G heads against the tile's
+// tokens, and P . V). On CUDA cores they made the split kernel issue-bound on GB300 (the
+// consumers alone, with no HBM traffic, took about as long as the whole kernel), so they run
+// on the tensor cores with warp-level m16n8k16 bf16 MMAs, in transposed form so that the 16
+// rows of the MMA are never wasted on a small group:
 //   S^T = K q^T: A = the warp's 16 K rows (8 of each of two stages) read with ldmatrix from
 //   the 128-byte-swizzled TMA tile, B = q^T (k = d, n = heads; unscaled bf16 so the operand is
 //   exact, the scale applied to the FP32 logits), 8 MMAs for d = 128;
 //   O^T += V^T P^T: A = V^T read with ldmatrix.trans (rows = d), B = P^T, which movmatrix
 //   transposes out of the S^T accumulator layout in registers; 8 m-tiles for d = 128.
+// The MMA's n = 8 head columns beyond the group are zero in q and masked in the softmax, so a
+// group of 1 or 2 heads costs the same instructions per KV byte as a group of 8.
 // O accumulates in the MMA registers across the whole piece. With one constant phi
 // (FlashDecoding++ Eq. 3 / Eq. 4) the accumulators are never rescaled. In the synchronised
 // mode each warp keeps a running maximum per head (the online-softmax recurrence of

@@ -112,8 +112,7 @@ typedef struct {
    * kv_fp8 = 1: k_cache and v_cache hold one-byte E4M3 codes (sign, 4-bit exponent with
    * bias 7, 3-bit mantissa, no infinities, S.1111.111 = NaN; "E4M3FN"), element for element
    * in the layout above, and code c stands for c * k_scale (K) or c * v_scale (V), scales
-   * finite and > 0; q stays qkv_dtype, which must be DA_BF16, and G must be 4 or 8 (else
-   * DA_ERR_UNSUPPORTED). The codes convert exactly; k_scale enters the logits' FP32 scale
+   * finite and > 0; q stays qkv_dtype, which must be DA_BF16 (else DA_ERR_UNSUPPORTED). The codes convert exactly; k_scale enters the logits' FP32 scale
    * factor and v_scale the output's. NaN codes are not detected (they read as finite
    * values). kv_fp8 = 0: k_cache and v_cache are qkv_dtype; the scales are not read. */
   int kv_fp8;

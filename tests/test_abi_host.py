@@ -57,19 +57,25 @@ def test_abi_version_and_strerror(L):
     (dict(mode="unified", unified_max=math.inf), -1),
     (dict(mode="unified_local", range_lo=1.0, range_hi=-1.0), -1),
     (dict(num_sms=-1), -1),
-    # FP8 caches: bf16 q, groups of 4 or 8, finite positive scales
+    # FP8 caches: bf16 q, finite positive scales
     (dict(kv_dtype="e4m3", k_scale=0.0), -1),
     (dict(kv_dtype="e4m3", v_scale=-1.0), -1),
     (dict(kv_dtype="e4m3", k_scale=math.inf), -1),
     (dict(kv_dtype="e4m3", v_scale=math.nan), -1),
     (dict(kv_dtype="e4m3", qkv_dtype="f16", out_dtype="f16"), -2),
-    (dict(kv_dtype="e4m3", num_q_heads=16, num_kv_heads=8), -2),   # G = 2
-    (dict(kv_dtype="e4m3", num_q_heads=8, num_kv_heads=8), -2),    # G = 1
+    (dict(debug_stall_stage=-1), -1),
 ])
 def test_plan_rejects_bad_problems(L, kw, code):
     with pytest.raises(binding.DecodeAttnError) as e:
         binding.decode_attn_plan(_prob(**kw), 0)
     assert e.value.code == code
+
+
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+def test_fp8_plans_for_every_group(L, group):
+    plan, _ = binding.decode_attn_plan(_prob(kv_dtype="e4m3", num_q_heads=8 * group,
+                                             num_kv_heads=8), 0)
+    binding.decode_attn_destroy(plan)
 
 
 def test_plan_rejects_a_bad_fp8_flag(L):

@@ -75,7 +75,7 @@ EDGE_LENS = (0, 1, 15, 16, 17, 63, 64, 65, 127, 129, 1000, 1024 + 7)
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("head_dim", [64, 128])
-@pytest.mark.parametrize("group", [4, 8])
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
 @pytest.mark.parametrize("page_size", [0, 16, 32])
 def test_fp8_edge_sweep(_gpu, head_dim, group, page_size):
     """Ragged and empty sequences, tails of every stage and page position, both head dims and
