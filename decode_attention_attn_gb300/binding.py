@@ -72,6 +72,7 @@ class da_plan_info(ctypes.Structure):
         ("smem_bytes", ctypes.c_size_t),
         ("split_tokens", ctypes.c_int),
         ("split_tokens_min", ctypes.c_int),
+        ("kv_heads_per_group", ctypes.c_int),
     ]
 
 

@@ -22,7 +22,7 @@ namespace da {
 const void* kernel_f32(int head_dim, int group, int mode);
 const void* kernel_f16(int head_dim, int group, int mode);
 const void* kernel_bf16(int head_dim, int group, int mode);
-const void* kernel_fp8(int head_dim, int group, int mode);
+const void* kernel_fp8(int head_dim, int group, int mode, int kv_heads);
 
 // The element offset the kernel reads token t of (b, kvh) from: the same token_row() the
 // producer warp uses for its TMA box coordinates.
@@ -229,6 +229,8 @@ struct da_plan {
   int num_sms;
   int group, es, unit, box_tokens, capacity, n_groups, piece_units;
   int kv_es;                    // K / V bytes per element (1: FP8 E4M3 cache; else es)
+  int hp;                       // KV heads per split-kernel group (2: packed FP8 pairs)
+  int sgroup;                   // query heads per split-kernel group (group * hp)
   int policy, num_splits;       // the plan's default split choice
   int narrow;                   // the device schedule's arithmetic fits 32 bits
   int grid;                     // balanced grid (or the default uniform grid)
@@ -305,11 +307,11 @@ int validate_problem(const da_problem& p) {
 }
 
 const void* kernel_for(const da_plan& pl, int mode) {
-  if (pl.prob.kv_fp8) return kernel_fp8(pl.prob.head_dim, pl.group, mode);
+  if (pl.prob.kv_fp8) return kernel_fp8(pl.prob.head_dim, pl.sgroup, mode, pl.hp);
   switch (pl.prob.qkv_dtype) {
-    case DA_F32: return kernel_f32(pl.prob.head_dim, pl.group, mode);
-    case DA_F16: return kernel_f16(pl.prob.head_dim, pl.group, mode);
-    case DA_BF16: return kernel_bf16(pl.prob.head_dim, pl.group, mode);
+    case DA_F32: return kernel_f32(pl.prob.head_dim, pl.sgroup, mode);
+    case DA_F16: return kernel_f16(pl.prob.head_dim, pl.sgroup, mode);
+    case DA_BF16: return kernel_bf16(pl.prob.head_dim, pl.sgroup, mode);
   }
   return nullptr;
 }
@@ -373,7 +375,8 @@ int make_kv_map(const da_plan& pl, const void* base, bool swizzled, CUtensorMap*
   const int es = pl.kv_es;
   const cuuint64_t strides[2] = {(cuuint64_t)p.head_dim * es,
                                  (cuuint64_t)p.num_kv_heads * p.head_dim * es};
-  const cuuint32_t box[3] = {(cuuint32_t)p.head_dim, 1u, (cuuint32_t)pl.box_tokens};
+  // a box holds the rows of the split kernel's hp KV heads of box_tokens tokens
+  const cuuint32_t box[3] = {(cuuint32_t)p.head_dim, (cuuint32_t)pl.hp, (cuuint32_t)pl.box_tokens};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   // L2 fills no wider than a KV row: with a wider promotion every box row also pulls in the
   // neighbouring head's row, which a paged gather seldom reads before it is evicted (FP8 rows
@@ -510,9 +513,24 @@ int decode_attn_plan(const da_problem* problem, int num_splits, da_plan** plan_o
   pl->unit = p.paged ? std::max(16, p.page_size) : 16;
   pl->box_tokens = p.paged ? std::min(p.page_size, kStageTokens) : kStageTokens;
   pl->capacity = p.paged ? p.max_blocks_per_seq * p.page_size : p.max_seq_len;
-  pl->n_groups = p.batch * p.num_kv_heads;
+  // FP8 caches with groups of 4 query heads over pairs of KV heads: the split kernel can take
+  // a pair at once (8 query heads, all of the tensor-core consumer's columns, and one 256-byte
+  // read of a token's two rows at d = 128). It does where the step is large: four packed
+  // groups per SM or more, or a cache of 128 MiB and more. On a smaller step spread over many
+  // CTAs per group, merging twice the partials of twice the heads costs more than the faster
+  // stream saves (batch 1, 8 KV heads: 6 us slower at 8K tokens, 10 us faster at 128K).
+  pl->hp = 1;
+  if (p.kv_fp8 && pl->group == 4 && p.num_kv_heads % 2 == 0) {
+    const long long packed = (long long)p.batch * (p.num_kv_heads / 2);
+    const long long cache_bytes =
+        2LL * p.batch * pl->capacity * p.num_kv_heads * p.head_dim;   // K + V, one byte each
+    if (packed * 4 >= sms || cache_bytes >= (128LL << 20)) pl->hp = 2;
+  }
+  pl->sgroup = pl->group * pl->hp;
+  pl->n_groups = p.batch * (p.num_kv_heads / pl->hp);
   {
-    const long long unit_bytes = 2LL * pl->unit * p.head_dim * pl->kv_es;   // K + V of one unit
+    // K + V of one unit of a group
+    const long long unit_bytes = 2LL * pl->unit * p.head_dim * pl->kv_es * pl->hp;
     pl->piece_units = (int)((kPieceCostBytes + unit_bytes / 2) / unit_bytes);
   }
   const long long units_max = (pl->capacity + pl->unit - 1) / pl->unit;
@@ -561,7 +579,8 @@ int decode_attn_plan(const da_problem* problem, int num_splits, da_plan** plan_o
   // deepest pipeline that fits the per-CTA shared memory limit
   pl->stages = 0;
   for (int s = kMaxStages; s >= 2; --s) {
-    const Layout L = make_layout(p.head_dim, pl->group, pl->es, s, pl->batch_smem, pl->kv_es);
+    const Layout L =
+        make_layout(p.head_dim, pl->sgroup, pl->es, s, pl->batch_smem, pl->kv_es, pl->hp);
     if (L.total <= kSmemLimit) {
       pl->stages = s;
       pl->smem_bytes = L.total;
@@ -575,7 +594,7 @@ int decode_attn_plan(const da_problem* problem, int num_splits, da_plan** plan_o
 
   // Workspace: the counters, the flagged list, status and statistics (zeroed once, left at
   // zero by every run), then the partials (no initial value needed).
-  const int G = pl->group, D = p.head_dim;
+  const int G = pl->sgroup, D = p.head_dim;
   size_t off = 0;
   pl->off_counters = off;
   off = align256(off + (size_t)pl->n_groups * 4);
@@ -646,6 +665,7 @@ int decode_attn_plan_info(const da_plan* plan, da_plan_info* info) {
   info->max_splits = plan->max_splits;
   info->workspace_bytes = plan->ws_bytes;
   info->smem_bytes = plan->smem_bytes;
+  info->kv_heads_per_group = plan->hp;
   return DA_OK;
 }
 
@@ -728,7 +748,7 @@ int decode_attn_run_ex(const da_plan* plan, const da_run_args* args) {
   const bool unified = p.mode == DA_SOFTMAX_UNIFIED;   // the recompute launch follows
 
   // tensor-core kernels (both modes, so the recompute pass too) read 128-byte-swizzled tiles
-  const bool mma = uses_mma(pl.kv_es, p.qkv_dtype == DA_F16, pl.group);
+  const bool mma = uses_mma(pl.kv_es, p.qkv_dtype == DA_F16, pl.sgroup);
   CUtensorMap tmk, tmv;
   int rc = make_kv_map(pl, k_cache, mma, &tmk);
   if (rc == DA_OK) rc = make_kv_map(pl, v_cache, mma, &tmv);
@@ -736,6 +756,8 @@ int decode_attn_run_ex(const da_plan* plan, const da_run_args* args) {
 
   Params kp;
   fill_common(pl, kp, block_table, seq_lens, workspace);
+  kp.hkv = p.num_kv_heads / pl.hp;   // the split kernel's groups (packed FP8: KV head pairs)
+  kp.group = pl.sgroup;
   kp.q = q;
   kp.out = out;
   kp.out_lse = out_lse;

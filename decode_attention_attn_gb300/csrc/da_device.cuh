@@ -49,16 +49,30 @@ enum OutType { kOutF32 = 0, kOutF16 = 1, kOutBF16 = 2 };
 
 // FP8 storage of K and V: one E4M3 code per element (sign, 4-bit exponent with bias 7, 3-bit
 // mantissa; no infinities), standing for code * k_scale or code * v_scale. q stays bf16.
-struct fp8e4m3 {
+// HP > 1: the split kernel's view of such a cache in which each group packs the query heads of
+// HP consecutive KV heads (a TMA box then holds HP rows of every token, see Cfg::kHp).
+template <int HP>
+struct fp8e4m3_heads {
   uint8_t bits;
 };
+using fp8e4m3 = fp8e4m3_heads<1>;
 template <typename T>
 struct QOf {   // q's storage type for a K / V storage type
   using type = T;
 };
-template <>
-struct QOf<fp8e4m3> {
+template <int HP>
+struct QOf<fp8e4m3_heads<HP>> {
   using type = __nv_bfloat16;
+};
+template <typename T>
+struct KvHeads {   // KV heads per group of the split kernel, and whether the cache is FP8
+  static constexpr int value = 1;
+  static constexpr bool fp8 = false;
+};
+template <int HP>
+struct KvHeads<fp8e4m3_heads<HP>> {
+  static constexpr int value = HP;
+  static constexpr bool fp8 = true;
 };
 
 struct Params {
@@ -147,11 +161,12 @@ __host__ __device__ constexpr int warp_scratch_floats(int D, int G, int es) {
   return (m + 3) / 4 * 4;
 }
 
-// es: q's bytes per element (also the consumer scratch geometry's); kv_es: K / V's (0: es).
+// es: q's bytes per element (also the consumer scratch geometry's); kv_es: K / V's (0: es);
+// hp: KV heads per group, whose rows a stage holds for every token.
 __host__ __device__ inline Layout make_layout(int D, int G, int es, int stages, int batch_smem,
-                                              int kv_es = 0) {
+                                              int kv_es = 0, int hp = 1) {
   Layout L;
-  const uint32_t kv = (uint32_t)kStageTokens * D * (kv_es ? kv_es : es);
+  const uint32_t kv = (uint32_t)kStageTokens * D * (kv_es ? kv_es : es) * (uint32_t)hp;
   L.k_off = 0;
   L.v_off = kv;
   L.q_off = 2 * kv;

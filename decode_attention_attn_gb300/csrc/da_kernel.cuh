@@ -46,7 +46,8 @@ namespace da {
 template <typename T, int D, int G>
 struct Cfg {
   using Q = typename QOf<T>::type;                    // q's storage (bf16 over FP8 K / V)
-  static constexpr bool kFp8 = std::is_same<T, fp8e4m3>::value;
+  static constexpr bool kFp8 = KvHeads<T>::fp8;
+  static constexpr int kHp = KvHeads<T>::value;         // KV heads per group (packed FP8: 2)
   static constexpr int kEs = sizeof(T);                 // K / V bytes per element
   static constexpr int kQEs = sizeof(Q);
   static constexpr int kEpl = 16 / kEs;               // elements per 16-byte chunk
@@ -56,7 +57,8 @@ struct Cfg {
   static constexpr int kV = G * kT;                   // logits per lane group per stage
   static constexpr int kNv = kV >= kLg ? kV / kLg : 1;    // complete logits per lane
   static constexpr int kRep = kV >= kLg ? 1 : kLg / kV;   // lanes that hold the same logit
-  static constexpr int kRowBytes = D * kEs;
+  static constexpr int kRowBytes = D * kEs;             // one KV head's row of a token
+  static constexpr int kTokBytes = kRowBytes * kHp;     // a token's rows in a stage tile
   static constexpr int kQBytes = G * D * kQEs;
   static_assert(kLg >= 1 && kLg <= 32 && (32 % kLg) == 0, "a row must span a lane group");
   static_assert((kTokensPerWarp % kNlg) == 0, "rows per warp must split over lane groups");
@@ -235,24 +237,24 @@ __device__ __forceinline__ void run_producer(const Params& p, Sched s, uint8_t* 
         }
         if (part == 0 && lane == 0 && !skip) {
           const uint32_t bytes =
-              (uint32_t)nbox * box * C::kRowBytes * 2u + (j == 0 ? (uint32_t)C::kQBytes : 0u);
+              (uint32_t)nbox * box * C::kTokBytes * 2u + (j == 0 ? (uint32_t)C::kQBytes : 0u);
           mbar_arrive_expect_tx(&full[slot], bytes);
           if (j == 0) bulk_load(st + L.q_off, qsrc, C::kQBytes, &full[slot]);
         }
         __syncwarp();
         if (bi < nbox && !skip) {
-          const uint32_t off = ((part & 1) == 0 ? L.k_off : L.v_off) + bi * box * C::kRowBytes;
+          const uint32_t off = ((part & 1) == 0 ? L.k_off : L.v_off) + bi * box * C::kTokBytes;
           const CUtensorMap* tm = (part & 1) == 0 ? tmk : tmv;
           if constexpr (SWZ)
             tma_load_4d(st + off, tm, &full[slot], 0, 0, pc.kvh, z, pol);
           else
-            tma_load_3d(st + off, tm, &full[slot], 0, pc.kvh, z, pol);
+            tma_load_3d(st + off, tm, &full[slot], 0, pc.kvh * C::kHp, z, pol);
         }
       } else if (lane == 0 && !skip) {
         const int z = pc.b * p.max_seq_len + ts;
         if (part == 0) {
           const uint32_t bytes =
-              (uint32_t)kStageTokens * C::kRowBytes * 2u + (j == 0 ? (uint32_t)C::kQBytes : 0u);
+              (uint32_t)kStageTokens * C::kTokBytes * 2u + (j == 0 ? (uint32_t)C::kQBytes : 0u);
           mbar_arrive_expect_tx(&full[slot], bytes);
           if (j == 0) bulk_load(st + L.q_off, qsrc, C::kQBytes, &full[slot]);
         }
@@ -261,7 +263,7 @@ __device__ __forceinline__ void run_producer(const Params& p, Sched s, uint8_t* 
         if constexpr (SWZ)
           tma_load_4d(st + off, tm, &full[slot], 0, 0, pc.kvh, z, pol);
         else
-          tma_load_3d(st + off, tm, &full[slot], 0, pc.kvh, z, pol);
+          tma_load_3d(st + off, tm, &full[slot], 0, pc.kvh * C::kHp, z, pol);
       }
       __syncwarp();
     }
@@ -991,7 +993,8 @@ __device__ __forceinline__ void run_consumers_mma(const Params& p, Sched s, uint
       const uint32_t vt[2] = {smem_u32(st0 + L.v_off), smem_u32(st1m + L.v_off)};
       if (!dead) {
         if constexpr (kFp8)
-          mma_consume_fp8<D, G, UNIFIED, LOCAL>(p, st, kt, vt, n, row0, lane, fmask);
+          mma_consume_fp8<D, G, Cfg<T, D, G>::kHp, UNIFIED, LOCAL>(p, st, kt, vt, n, row0, lane,
+                                                                    fmask);
         else
           mma_consume<D, G, UNIFIED, LOCAL>(p, st, mlane, kt, vt, n, row0, lane, fmask);
       }
@@ -1068,7 +1071,7 @@ __device__ __forceinline__ void consumer_role(const Params& p, int warp, int lan
   using C = Cfg<T, D, G>;
   constexpr bool kMma = uses_mma(sizeof(T), std::is_same<T, __half>::value, G);
   uint8_t* smem = smem_base();
-  const Layout L = make_layout(D, G, C::kQEs, p.stages, p.batch_smem, C::kEs);
+  const Layout L = make_layout(D, G, C::kQEs, p.stages, p.batch_smem, C::kEs, C::kHp);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   uint64_t* empty = full + p.stages;
   const Sched s = launch_sched(p, reinterpret_cast<const int*>(smem + L.lens_off),
@@ -1090,7 +1093,7 @@ __device__ __forceinline__ void producer_role(const Params& p, const CUtensorMap
   constexpr bool k4d = kMma && !C::kFp8;   // bf16 tensor-core tiles: the 4-D swizzled view
   if (warp >= kConsumerWarps + (p.paged ? 4 : 2)) return;
   uint8_t* smem = smem_base();
-  const Layout L = make_layout(D, G, C::kQEs, p.stages, p.batch_smem, C::kEs);
+  const Layout L = make_layout(D, G, C::kQEs, p.stages, p.batch_smem, C::kEs, C::kHp);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   uint64_t* empty = full + p.stages;
   const Sched s = launch_sched(p, reinterpret_cast<const int*>(smem + L.lens_off),
@@ -1121,7 +1124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   {
     uint8_t* smem = smem_base();
-    const Layout L = make_layout(D, G, C::kQEs, p.stages, p.batch_smem, C::kEs);
+    const Layout L = make_layout(D, G, C::kQEs, p.stages, p.batch_smem, C::kEs, C::kHp);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
     uint64_t* empty = full + p.stages;
     int* lens = reinterpret_cast<int*>(smem + L.lens_off);
@@ -1234,22 +1237,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+template <typename T, int D, int G>
+inline const void* pick_mode(int mode) {
+  return mode == kSoftmaxSync      ? (const void*)&decode_split_kernel<T, D, G, 0>
+         : mode == kSoftmaxUnified ? (const void*)&decode_split_kernel<T, D, G, 1>
+                                   : (const void*)&decode_split_kernel<T, D, G, 2>;
+}
+
 template <typename T, int D>
 inline const void* pick_kernel(int G, int mode) {
-#define DA_CASE(GG)                                                                      \
-  case GG:                                                                               \
-    return mode == kSoftmaxSync      ? (const void*)&decode_split_kernel<T, D, GG, 0>    \
-           : mode == kSoftmaxUnified ? (const void*)&decode_split_kernel<T, D, GG, 1>    \
-                                     : (const void*)&decode_split_kernel<T, D, GG, 2>;
   switch (G) {
-    DA_CASE(1)
-    DA_CASE(2)
-    DA_CASE(4)
-    DA_CASE(8)
-    default:
-      return nullptr;
+    case 1: return pick_mode<T, D, 1>(mode);
+    case 2: return pick_mode<T, D, 2>(mode);
+    case 4: return pick_mode<T, D, 4>(mode);
+    case 8: return pick_mode<T, D, 8>(mode);
+    default: return nullptr;
   }
-#undef DA_CASE
 }
 
 

@@ -22,6 +22,8 @@
 // keeps P exact to ~2^-17; the softmax denominators are summed from the FP32 p.
 #pragma once
 
+#include <type_traits>
+
 #include "da_device.cuh"
 
 namespace da {
@@ -109,15 +111,15 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return r;
 }
 
-// Byte offset of 16-byte chunk c of token row t in an FP8 tile of 64 rows of D bytes, as the
-// TMA box writes it: with the 128-byte swizzle for D = 128 (chunk c of row t at chunk
-// c ^ (t mod 8)), unswizzled for D = 64.
+// Byte offset of 16-byte chunk c of row r in an FP8 tile of rows of D bytes (row t * HP + h
+// holds KV head h of token t), as the TMA box writes it: with the 128-byte swizzle for
+// D = 128 (chunk c of row r at chunk c ^ (r mod 8)), unswizzled for D = 64.
 template <int D>
-__device__ __forceinline__ uint32_t fp8_off(int t, int c) {
+__device__ __forceinline__ uint32_t fp8_off(int r, int c) {
   if constexpr (D == 128)
-    return (uint32_t)(t * 128 + ((c ^ (t & 7)) << 4));
+    return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
   else
-    return (uint32_t)(t * D + c * 16);
+    return (uint32_t)(r * D + c * 16);
 }
 
 // Byte offset of element e (a multiple of 8) of row t in a tile written by a TMA box of
@@ -433,38 +435,47 @@ __device__ __forceinline__ void mma_load_q_fp8(const Params& p, MmaState<D, G>& 
   st.qmul = p.qscale * down;
 }
 
-// mma_consume over FP8 tiles (kt / vt, n, row0 as there).
-template <int D, int G, bool UNIFIED, bool LOCAL>
+// mma_consume over FP8 tiles (kt / vt, n, row0 as there). HP > 1: the tiles hold HP KV heads'
+// rows of every token (row t * HP + h) and the group's G columns are HP blocks of G / HP query
+// heads, one block per KV head. Each contraction then runs once per KV head with the other
+// heads' columns of its B operand zeroed, so that all of them add into the same accumulators:
+// S^T = sum_h K_h [q^T, head h's columns], O^T += sum_h V_h^T [P^T, head h's columns]. The
+// MMA's 8 columns are then all in use, where an unpacked group of 4 heads leaves half of them
+// (and of the softmax work) idle.
+template <int D, int G, int HP, bool UNIFIED, bool LOCAL>
 __device__ __forceinline__ void mma_consume_fp8(const Params& p, MmaState<D, G>& st,
                                                 const uint32_t (&kt)[2], const uint32_t (&vt)[2],
                                                 const int (&n)[2], int row0, int lane,
                                                 uint32_t& fmask) {
+  static_assert(G % HP == 0, "every KV head has the same number of query heads");
   constexpr int KS = MmaState<D, G>::KS;
   constexpr int KW = D / 16;   // 4-byte words of a lane's K bytes (one per k-step)
   const int g = lane >> 2, c = lane & 3;
+  const int bh = g / (G / HP);   // KV head of this lane's B column (query head g)
 
-  // S^T = K q^T: A rows 0-7 = token row0 + g of stage 0, rows 8-15 = the same of stage 1
-  uint32_t k0[KW], k1[KW];
-  {
-    const int t = row0 + g;
-#pragma unroll
-    for (int h = 0; h < D / 64; ++h) {   // 16-byte chunks c * D/64 + h of the row
-      const uint4 w0 = lds128(kt[0] + fp8_off<D>(t, c * (D / 64) + h));
-      const uint4 w1 = lds128(kt[1] + fp8_off<D>(t, c * (D / 64) + h));
-      k0[4 * h] = w0.x; k0[4 * h + 1] = w0.y; k0[4 * h + 2] = w0.z; k0[4 * h + 3] = w0.w;
-      k1[4 * h] = w1.x; k1[4 * h + 1] = w1.y; k1[4 * h + 2] = w1.z; k1[4 * h + 3] = w1.w;
-    }
-  }
+  // S^T = K q^T: A rows 0-7 = token row0 + g of stage 0, rows 8-15 = the same of stage 1;
+  // two accumulator chains (even and odd k-steps), shared by the KV heads
   float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int kk = 0; kk < KS; ++kk) {
-    uint32_t a0, a1, a2, a3;
-    e4m3x4_to_f16x2(k0[kk], a0, a2);
-    e4m3x4_to_f16x2(k1[kk], a1, a3);
-    if (kk & 1)
-      mma_f16(sb, a0, a1, a2, a3, st.qb[kk][0], st.qb[kk][1]);
-    else
-      mma_f16(sa, a0, a1, a2, a3, st.qb[kk][0], st.qb[kk][1]);
+  for (int h = 0; h < HP; ++h) {
+    uint32_t k0[KW], k1[KW];
+    const int r = (row0 + g) * HP + h;
+#pragma unroll
+    for (int x = 0; x < D / 64; ++x) {   // 16-byte chunks c * D/64 + x of the row
+      const uint4 w0 = lds128(kt[0] + fp8_off<D>(r, c * (D / 64) + x));
+      const uint4 w1 = lds128(kt[1] + fp8_off<D>(r, c * (D / 64) + x));
+      k0[4 * x] = w0.x; k0[4 * x + 1] = w0.y; k0[4 * x + 2] = w0.z; k0[4 * x + 3] = w0.w;
+      k1[4 * x] = w1.x; k1[4 * x + 1] = w1.y; k1[4 * x + 2] = w1.z; k1[4 * x + 3] = w1.w;
+    }
+    const bool on = HP == 1 || bh == h;
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      uint32_t a0, a1, a2, a3;
+      e4m3x4_to_f16x2(k0[kk], a0, a2);
+      e4m3x4_to_f16x2(k1[kk], a1, a3);
+      mma_f16((kk & 1) ? sb : sa, a0, a1, a2, a3, on ? st.qb[kk][0] : 0u,
+              on ? st.qb[kk][1] : 0u);
+    }
   }
   uint32_t bh0, bh1, bl0, bl1, vm0, vm1;
   float f0, f1;
@@ -475,56 +486,70 @@ __device__ __forceinline__ void mma_consume_fp8(const Params& p, MmaState<D, G>&
   const bool tail = (vm0 & vm1) != 0xffffffffu;
 
   // O^T += V^T P^T: the lane's D/8 bytes (d = (D/8) g + 0 .. D/8 - 1) of tokens row0 + 2c and
-  // row0 + 2c + 1 of both stages; word w of a row covers m-tiles 2w and 2w + 1
+  // row0 + 2c + 1 of both stages, for every KV head; word w of a row covers m-tiles 2w and
+  // 2w + 1
   constexpr int VW = D / 32;   // 4-byte words per row and lane
-  uint32_t va[VW], vb[VW], vc[VW], vd[VW];
-  {
+  uint32_t va[HP][VW], vb[HP][VW], vc[HP][VW], vd[HP][VW];
+#pragma unroll
+  for (int h = 0; h < HP; ++h) {
     const int t = row0 + 2 * c;
+    const int r0 = t * HP + h, r1 = (t + 1) * HP + h;
     if constexpr (D == 128) {
-      const uint4 x = lds128(vt[0] + fp8_off<D>(t, g)), y = lds128(vt[0] + fp8_off<D>(t + 1, g));
-      const uint4 z = lds128(vt[1] + fp8_off<D>(t, g)), u = lds128(vt[1] + fp8_off<D>(t + 1, g));
-      va[0] = x.x; va[1] = x.y; va[2] = x.z; va[3] = x.w;
-      vb[0] = y.x; vb[1] = y.y; vb[2] = y.z; vb[3] = y.w;
-      vc[0] = z.x; vc[1] = z.y; vc[2] = z.z; vc[3] = z.w;
-      vd[0] = u.x; vd[1] = u.y; vd[2] = u.z; vd[3] = u.w;
+      const uint4 x = lds128(vt[0] + fp8_off<D>(r0, g)), y = lds128(vt[0] + fp8_off<D>(r1, g));
+      const uint4 z = lds128(vt[1] + fp8_off<D>(r0, g)), u = lds128(vt[1] + fp8_off<D>(r1, g));
+      va[h][0] = x.x; va[h][1] = x.y; va[h][2] = x.z; va[h][3] = x.w;
+      vb[h][0] = y.x; vb[h][1] = y.y; vb[h][2] = y.z; vb[h][3] = y.w;
+      vc[h][0] = z.x; vc[h][1] = z.y; vc[h][2] = z.z; vc[h][3] = z.w;
+      vd[h][0] = u.x; vd[h][1] = u.y; vd[h][2] = u.z; vd[h][3] = u.w;
     } else {
       const uint32_t o = (uint32_t)(8 * g);
-      const uint2 x = lds64(vt[0] + t * D + o), y = lds64(vt[0] + (t + 1) * D + o);
-      const uint2 z = lds64(vt[1] + t * D + o), u = lds64(vt[1] + (t + 1) * D + o);
-      va[0] = x.x; va[1] = x.y;
-      vb[0] = y.x; vb[1] = y.y;
-      vc[0] = z.x; vc[1] = z.y;
-      vd[0] = u.x; vd[1] = u.y;
+      const uint2 x = lds64(vt[0] + r0 * D + o), y = lds64(vt[0] + r1 * D + o);
+      const uint2 z = lds64(vt[1] + r0 * D + o), u = lds64(vt[1] + r1 * D + o);
+      va[h][0] = x.x; va[h][1] = x.y;
+      vb[h][0] = y.x; vb[h][1] = y.y;
+      vc[h][0] = z.x; vc[h][1] = z.y;
+      vd[h][0] = u.x; vd[h][1] = u.y;
     }
   }
+  // the unified phase scales each stage pair's P . V by f into the accumulators; the branch is
+  // taken once per stage pair, outside the m-tile loop
+  auto pv = [&](auto scaled_tag) {
+    constexpr bool SC = decltype(scaled_tag)::value;
 #pragma unroll
-  for (int mt = 0; mt < KS; ++mt) {
-    // bytes [token 2c, token 2c + 1] of d (the lower half) and of d + 1 (the upper half)
-    const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
-    const uint32_t x0 = prmt(va[mt >> 1], vb[mt >> 1], sel);
-    const uint32_t x1 = prmt(vc[mt >> 1], vd[mt >> 1], sel);
-    uint32_t a0, a1, a2, a3;
-    e4m3x4_to_f16x2(x0, a0, a1);
-    e4m3x4_to_f16x2(x1, a2, a3);
-    if (tail) {
-      a0 &= vm0;
-      a1 &= vm0;
-      a2 &= vm1;
-      a3 &= vm1;
-    }
-    if (scaled) {
+    for (int mt = 0; mt < KS; ++mt) {
+      // bytes [token 2c, token 2c + 1] of d (the lower half) and of d + 1 (the upper half)
+      const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
       float t4[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_f16(t4, a0, a1, a2, a3, bh0, bh1);
-      mma_f16(t4, a0, a1, a2, a3, bl0, bl1);
-      st.o[mt][0] = fmaf(f0, t4[0], st.o[mt][0]);
-      st.o[mt][1] = fmaf(f1, t4[1], st.o[mt][1]);
-      st.o[mt][2] = fmaf(f0, t4[2], st.o[mt][2]);
-      st.o[mt][3] = fmaf(f1, t4[3], st.o[mt][3]);
-    } else {
-      mma_f16(st.o[mt], a0, a1, a2, a3, bh0, bh1);
-      mma_f16(st.o[mt], a0, a1, a2, a3, bl0, bl1);
+      float (&acc)[4] = SC ? t4 : st.o[mt];
+#pragma unroll
+      for (int h = 0; h < HP; ++h) {
+        const uint32_t x0 = prmt(va[h][mt >> 1], vb[h][mt >> 1], sel);
+        const uint32_t x1 = prmt(vc[h][mt >> 1], vd[h][mt >> 1], sel);
+        uint32_t a0, a1, a2, a3;
+        e4m3x4_to_f16x2(x0, a0, a1);
+        e4m3x4_to_f16x2(x1, a2, a3);
+        if (tail) {
+          a0 &= vm0;
+          a1 &= vm0;
+          a2 &= vm1;
+          a3 &= vm1;
+        }
+        const uint32_t pm = HP == 1 || bh == h ? 0xffffffffu : 0u;   // this head's columns
+        mma_f16(acc, a0, a1, a2, a3, bh0 & pm, bh1 & pm);
+        mma_f16(acc, a0, a1, a2, a3, bl0 & pm, bl1 & pm);
+      }
+      if constexpr (SC) {
+        st.o[mt][0] = fmaf(f0, t4[0], st.o[mt][0]);
+        st.o[mt][1] = fmaf(f1, t4[1], st.o[mt][1]);
+        st.o[mt][2] = fmaf(f0, t4[2], st.o[mt][2]);
+        st.o[mt][3] = fmaf(f1, t4[3], st.o[mt][3]);
+      }
     }
-  }
+  };
+  if (scaled)
+    pv(std::true_type{});
+  else
+    pv(std::false_type{});
 }
 
 }  // namespace da

@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define DECODE_ATTN_ABI_VERSION 3
+#define DECODE_ATTN_ABI_VERSION 4
 
 /* Largest bin count decode_attn_logit_histogram accepts. */
 #define DECODE_ATTN_MAX_HIST_BINS 32768
@@ -112,7 +112,10 @@ typedef struct {
    * kv_fp8 = 1: k_cache and v_cache hold one-byte E4M3 codes (sign, 4-bit exponent with
    * bias 7, 3-bit mantissa, no infinities, S.1111.111 = NaN; "E4M3FN"), element for element
    * in the layout above, and code c stands for c * k_scale (K) or c * v_scale (V), scales
-   * finite and > 0; q stays qkv_dtype, which must be DA_BF16 (else DA_ERR_UNSUPPORTED). The codes convert exactly; k_scale enters the logits' FP32 scale
+   * finite and > 0; q stays qkv_dtype, which must be DA_BF16 (else DA_ERR_UNSUPPORTED).
+   * With groups of 4 query heads over an even number of KV heads, the plan packs pairs of KV
+   * heads into one group of the split kernel where the step is large (at least four packed
+   * groups per SM, or a cache capacity of 128 MiB and more); da_plan_info reports it. The codes convert exactly; k_scale enters the logits' FP32 scale
    * factor and v_scale the output's. NaN codes are not detected (they read as finite
    * values). kv_fp8 = 0: k_cache and v_cache are qkv_dtype; the scales are not read. */
   int kv_fp8;
@@ -145,6 +148,10 @@ typedef struct {
                                step whose sequences are all at capacity, under the plan's
                                default policy ("the split size" of Flash-Decoding) */
   int split_tokens_min;     /* smallest such split */
+  int kv_heads_per_group;   /* KV heads one split-kernel group reads together: 2 where an FP8
+                               cache's groups of 4 query heads are packed in pairs of KV heads
+                               (8 query heads fill the tensor-core consumer; see kv_fp8), else
+                               1. Splits, partials and the merge are then per pair. */
 } da_plan_info;
 
 /* Filled by decode_attn_run when requested (forces a stream synchronisation). */

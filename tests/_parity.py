@@ -58,13 +58,13 @@ def run_oracle(inp: workloads.Inputs, rows=None, nthreads=None, phi=None, lo=Non
 
 
 def run_gpu(dev: DeviceInputs, mode=None, num_splits=None, out_dtype=None, plan_splits=None,
-            validate=False, want_stats=False, phi=None, lo=None, hi=None, attn=None):
+            validate=False, want_stats=False, phi=None, lo=None, hi=None, attn=None, num_sms=0):
     inp = dev.inp
     w = inp.wl
     if attn is None:
         ns = w.num_splits if plan_splits is None else plan_splits
-        attn = binding.DecodeAttention(problem_for(inp, mode, out_dtype, validate, phi, lo, hi),
-                                       ns)
+        attn = binding.DecodeAttention(
+            problem_for(inp, mode, out_dtype, validate, phi, lo, hi, num_sms), ns)
     res = attn.run(dev.q, dev.k, dev.v, dev.bt, dev.sl, w.scale,
                    -1 if num_splits is None else num_splits, want_stats=want_stats)
     torch.cuda.synchronize()

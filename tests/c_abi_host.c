@@ -48,9 +48,9 @@ int main(void) {
     rc = decode_attn_plan_info(plan, &info);
     if (rc != DA_OK) return fail("plan_info", rc);
     if (info.workspace_bytes != ws) return fail("workspace bytes", 0);
-    printf("%s grid_ctas %d stages %d stage_tokens %d workspace %zu smem %zu\n",
+    printf("%s grid_ctas %d stages %d stage_tokens %d workspace %zu smem %zu kv_heads %d\n",
            fp8 ? "fp8" : "bf16", info.grid_ctas, info.stages, info.stage_tokens,
-           info.workspace_bytes, info.smem_bytes);
+           info.workspace_bytes, info.smem_bytes, info.kv_heads_per_group);
     /* a run with null inputs is refused on the host */
     rc = decode_attn_run(plan, NULL, NULL, NULL, NULL, NULL, 0.088f, -1, NULL, NULL, NULL, NULL,
                          0, NULL, NULL);

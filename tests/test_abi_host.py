@@ -35,7 +35,7 @@ def test_library_exports_every_header_symbol(L):
 
 
 def test_abi_version_and_strerror(L):
-    assert binding.decode_attn_abi_version() == 3
+    assert binding.decode_attn_abi_version() == 4
     for code in binding.ERRORS:
         assert binding.decode_attn_strerror(code)
     assert "unknown" in binding.decode_attn_strerror(-99)
@@ -86,20 +86,36 @@ def test_plan_rejects_a_bad_fp8_flag(L):
     assert e.value.code == -1
 
 
-def test_fp8_plan_halves_the_stage_and_the_piece_cost(L):
-    """An FP8 cache moves one byte per K / V element: the stages hold the same 64 tokens in
-    less shared memory (so the pipeline is at least as deep), and a piece's fixed cost is
-    charged in twice as many 16-token units."""
-    plan16, _ = binding.decode_attn_plan(_prob(), 0)
-    plan8, _ = binding.decode_attn_plan(_prob(kv_dtype="e4m3", k_scale=0.01, v_scale=0.02), 0)
-    try:
-        i16, i8 = binding.decode_attn_plan_info(plan16), binding.decode_attn_plan_info(plan8)
-        assert i8.stage_tokens == i16.stage_tokens == 64
-        assert i8.stages >= i16.stages and i8.smem_bytes <= 232448
-        assert i8.grid_ctas == i16.grid_ctas == 152
-    finally:
-        binding.decode_attn_destroy(plan16)
-        binding.decode_attn_destroy(plan8)
+def test_fp8_plan_packs_kv_head_pairs_on_large_steps(L):
+    """FP8 caches with groups of 4 query heads over pairs of KV heads: the split kernel takes a
+    pair at once where the step is large (four packed groups per SM, or 128 MiB of cache), so
+    that its 64-token stage holds as many bytes as a bf16 stage of one KV head and a balanced
+    share covers half as many tokens of a group. The 32K GQA step (67 MB) keeps one KV head
+    per group, with half-size stages and a deeper pipeline; so does an odd KV-head count."""
+    fp8 = dict(kv_dtype="e4m3", k_scale=0.01, v_scale=0.02)
+    paged = dict(batch=64, paged=True, page_size=16, max_blocks_per_seq=512,
+                 num_physical_blocks=20000, max_seq_len=0)
+    cases = {"bf16": _prob(), "32k": _prob(**fp8), "128k": _prob(max_seq_len=131072, **fp8),
+             "paged": _prob(**paged, **fp8), "odd": _prob(num_q_heads=12, num_kv_heads=3, **fp8),
+             "odd_paged": _prob(**paged, num_q_heads=12, num_kv_heads=3, **fp8),
+             "few_sms": _prob(num_sms=16, **fp8)}
+    info = {}
+    for k, prob in cases.items():
+        plan, _ = binding.decode_attn_plan(prob, 0)
+        info[k] = binding.decode_attn_plan_info(plan)
+        binding.decode_attn_destroy(plan)
+    hp = {k: i.kv_heads_per_group for k, i in info.items()}
+    assert hp == {"bf16": 1, "32k": 1, "128k": 2, "paged": 2, "odd": 1, "odd_paged": 1,
+                  "few_sms": 2}
+    for k, i in info.items():
+        assert i.stage_tokens == 64 and i.smem_bytes <= 232448
+    assert info["32k"].stages > info["bf16"].stages
+    assert info["128k"].stages >= 5
+    # a packed share: half the tokens of a pair that carries twice the bytes per token
+    s16, _ = binding.decode_attn_plan(_prob(max_seq_len=131072), 0)
+    i16 = binding.decode_attn_plan_info(s16)
+    binding.decode_attn_destroy(s16)
+    assert abs(2 * info["128k"].split_tokens - i16.split_tokens) <= 64
 
 
 def test_plan_rejects_an_unknown_softmax_mode(L):
@@ -288,3 +304,4 @@ def test_plain_c_program_uses_the_abi(L, tmp_path):
     fp8 = next(x for x in lines if x.startswith("fp8 ")).split()
     assert int(bf16[2]) == int(fp8[2]) == 152                # grid_ctas
     assert int(fp8[4]) >= int(bf16[4])                       # stages: FP8 tiles are smaller
+    assert int(bf16[12]) == int(fp8[12]) == 1                # 32K GQA: one KV head per group

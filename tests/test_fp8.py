@@ -17,10 +17,11 @@ from decode_attention_attn_gb300 import binding, build as lib_build, workloads
 W = workloads
 
 
-def _check(dev, ref, ref_lse, mode, out_dtype=None, num_splits=None, plan_splits=None, where=""):
+def _check(dev, ref, ref_lse, mode, out_dtype=None, num_splits=None, plan_splits=None, where="",
+           num_sms=0):
     od = out_dtype or dev.inp.wl.out_dtype
     out, lse, flags = _parity.run_gpu(dev, mode=mode, out_dtype=od, num_splits=num_splits,
-                                      plan_splits=plan_splits)
+                                      plan_splits=plan_splits, num_sms=num_sms)
     _parity.compare(out, ref.reshape(out.shape), od, where=f"{where} {mode} {od}")
     _parity.compare_lse(lse, ref_lse.reshape(lse.shape), where=f"{where} {mode}")
     return out, lse, flags
@@ -50,7 +51,12 @@ def paged64_fp8(_gpu):
 @pytest.mark.gpu
 @pytest.mark.parametrize("mode", ["sync", "unified", "unified_local"])
 def test_gqa_32k_fp8(gqa32k_fp8, mode):
+    """One KV head per split-kernel group at this size (4 packed groups would spread over 38
+    CTAs each); the packed form of the same step is checked as well."""
     dev, (ref, ref_lse, ref_flag, margin) = gqa32k_fp8
+    plan = binding.DecodeAttention(_parity.problem_for(dev.inp, mode=mode), 0)
+    assert plan.info.kv_heads_per_group == 1
+    _check(dev, ref, ref_lse, mode, out_dtype="f32", num_sms=16, where="gqa32k fp8 packed")
     out, lse, flags = _check(dev, ref, ref_lse, mode, where="gqa32k fp8")
     _check(dev, ref, ref_lse, mode, out_dtype="f32", where="gqa32k fp8 fp32-out")
     _check(dev, ref, ref_lse, mode, num_splits=16, plan_splits=16, out_dtype="f32",
@@ -63,7 +69,10 @@ def test_gqa_32k_fp8(gqa32k_fp8, mode):
 @pytest.mark.gpu
 @pytest.mark.parametrize("mode", ["sync", "unified", "unified_local"])
 def test_paged_batch64_fp8(paged64_fp8, mode):
+    """The paged batch packs pairs of KV heads (256 packed groups on 152 SMs)."""
     dev, (ref, ref_lse, ref_flag, margin) = paged64_fp8
+    plan = binding.DecodeAttention(_parity.problem_for(dev.inp, mode=mode), 0)
+    assert plan.info.kv_heads_per_group == 2
     _check(dev, ref, ref_lse, mode, where="paged b64 fp8")
     _check(dev, ref, ref_lse, mode, out_dtype="f32", where="paged b64 fp8 fp32-out")
     _check(dev, ref, ref_lse, mode, num_splits=4, plan_splits=4, out_dtype="f32",
@@ -79,7 +88,9 @@ EDGE_LENS = (0, 1, 15, 16, 17, 63, 64, 65, 127, 129, 1000, 1024 + 7)
 @pytest.mark.parametrize("page_size", [0, 16, 32])
 def test_fp8_edge_sweep(_gpu, head_dim, group, page_size):
     """Ragged and empty sequences, tails of every stage and page position, both head dims and
-    groups, contiguous and paged caches, every mode and split choice."""
+    groups, contiguous and paged caches, every mode and split choice. Groups of 4 run twice:
+    planned for the device (one KV head per split-kernel group at this size) and for 32 SMs,
+    where the plan packs the two KV heads into one group."""
     paged = page_size > 0
     wl = W.Workload(f"fp8_edge_{head_dim}_{group}_{page_size}", len(EDGE_LENS), 2 * group, 2,
                     head_dim, "bf16", "bf16", lens=EDGE_LENS, paged=paged,
@@ -88,11 +99,34 @@ def test_fp8_edge_sweep(_gpu, head_dim, group, page_size):
     inp = W.generate(wl, offset=5 * group + head_dim + page_size)
     dev = _parity.DeviceInputs(inp)
     ref, ref_lse, _, _ = _parity.run_oracle(inp)
-    for i, mode in enumerate(("sync", "unified", "unified_local")):
-        for ns in ((0, 3), (1, 7), (0, 2))[i]:
-            for od in ("bf16", "f32"):
-                _check(dev, ref, ref_lse, mode, out_dtype=od, num_splits=ns, plan_splits=ns,
-                       where=f"fp8 edge d{head_dim} G{group} page={page_size} S={ns}")
+    for sms in ((0, 32) if group == 4 else (0,)):
+        packed = binding.DecodeAttention(_parity.problem_for(inp, num_sms=sms), 0)
+        assert packed.info.kv_heads_per_group == (2 if sms else 1)
+        for i, mode in enumerate(("sync", "unified", "unified_local")):
+            for ns in ((0, 3), (1, 7), (0, 2))[i]:
+                for od in ("bf16", "f32"):
+                    _check(dev, ref, ref_lse, mode, out_dtype=od, num_splits=ns, plan_splits=ns,
+                           num_sms=sms, where=f"fp8 edge d{head_dim} G{group} page={page_size} "
+                                              f"S={ns} sms={sms}")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("head_dim", [64, 128])
+@pytest.mark.parametrize("page_size", [0, 16])
+def test_fp8_group4_odd_kv_heads(_gpu, head_dim, page_size):
+    """Groups of 4 query heads over an odd number of KV heads: the last KV head has no partner,
+    so the plan keeps one KV head per group (the packed pairs cover an even count)."""
+    paged = page_size > 0
+    wl = W.Workload(f"fp8_odd_{head_dim}_{page_size}", 3, 12, 3, head_dim, "bf16", "bf16",
+                    lens=(1000, 65, 0), paged=paged, page_size=page_size or 16,
+                    max_seq_len=0 if paged else 1030, kv_dtype="e4m3")
+    inp = W.generate(wl, offset=11 + head_dim + page_size)
+    dev = _parity.DeviceInputs(inp)
+    ref, ref_lse, _, _ = _parity.run_oracle(inp)
+    for mode in ("sync", "unified", "unified_local"):
+        for ns in (0, 3):
+            _check(dev, ref, ref_lse, mode, out_dtype="f32", num_splits=ns, plan_splits=ns,
+                   where=f"fp8 odd kv heads d{head_dim} page={page_size} S={ns}")
 
 
 @pytest.mark.gpu
