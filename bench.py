@@ -288,7 +288,8 @@ def launches_per_step(mode):
 # (workload, softmax mode, split override): the MHA step runs with its stated 16 splits of
 # 256 tokens and once more with the library's balanced shares (None: the workload's own).
 SIDE_WORKLOADS = [("mha", "unified_local", None), ("mha", "unified_local", 0),
-                  ("paged", "unified_local", None), ("stress", "unified", None),
+                  ("paged", "unified_local", None), ("paged", "unified", None),
+                  ("stress", "unified", None),
                   ("stress", "unified_local", None), ("gqa32k_fp8", "unified_local", None),
                   ("paged_fp8", "unified_local", None)]
 
