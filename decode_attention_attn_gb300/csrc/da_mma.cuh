@@ -223,15 +223,36 @@ __device__ __forceinline__ void mma_softmax(const Params& p, MmaState<D, G>& st,
       for (int c = 0; c < 4; ++c) {
         if (valid[c]) {
           out = out || x[c] < p.lo2 || x[c] > p.hi2;
-          st.mt[c & 1] = fmaxf(st.mt[c & 1], x[c]);
+          if constexpr (F16) st.mt[c & 1] = fmaxf(st.mt[c & 1], x[c]);
         }
       }
       if (__any_sync(0xffffffffu, out)) {
-        float m0 = st.mt[0], m1 = st.mt[1];
+        // The new reference must bound every logit so far from above. f16 P (FP8 tiles) needs
+        // the maximum itself, kept per lane. With bf16 P a bound within log2(tokens) of it is
+        // as good, and the state gives one for free: its denominators are sums of 2^(x - phi)
+        // over in-range logits, so phi + log2(sum) lies between the maximum and the maximum
+        // plus log2 of the warp's token count.
+        float m0, m1;
+        if constexpr (F16) {
+          m0 = st.mt[0];
+          m1 = st.mt[1];
+        } else {
+          m0 = st.den[0];
+          m1 = st.den[1];
+        }
 #pragma unroll
         for (int o = 4; o <= 16; o <<= 1) {
-          m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
-          m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+          if constexpr (F16) {
+            m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+            m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+          } else {
+            m0 += __shfl_xor_sync(0xffffffffu, m0, o);
+            m1 += __shfl_xor_sync(0xffffffffu, m1, o);
+          }
+        }
+        if constexpr (!F16) {
+          m0 = m0 > 0.f ? p.phi2 + fast_log2(m0) : -INFINITY;
+          m1 = m1 > 0.f ? p.phi2 + fast_log2(m1) : -INFINITY;
         }
         const float al0 = m0 > -INFINITY ? fast_exp2(p.phi2 - m0) : 1.f;
         const float al1 = m1 > -INFINITY ? fast_exp2(p.phi2 - m1) : 1.f;
