@@ -197,6 +197,28 @@ def test_logit_histogram_accumulates_and_counts_the_tails():
 
 
 @pytest.mark.gpu
+def test_logit_histogram_skips_pages_outside_the_pool():
+    """A block-table entry outside the pool: its page's tokens are not counted, while the other
+    pages of the same 64-token item are. The page is each sequence's last, so the expected
+    counts are the oracle's over the sequences cut at that page's first token."""
+    wl = W.Workload("calib_bad_pages", 3, 8, 2, 128, "bf16", "bf16", lens=(200, 77, 1000),
+                    paged=True, page_size=16)
+    inp = W.generate(wl, offset=4)
+    dev = _parity.DeviceInputs(inp)
+    attn = binding.DecodeAttention(_parity.problem_for(inp, mode="sync"), 0)
+    cut = inp.seq_lens.clone()
+    for b, n in enumerate(inp.seq_lens.tolist()):
+        last = (n - 1) // wl.page_size
+        dev.bt[b, last] = inp.num_physical_blocks + 3 if b != 1 else -7
+        cut[b] = last * wl.page_size
+    counts = _device_histogram(attn, dev, wl.scale).cpu().numpy()
+    bt = inp.block_table.numpy()
+    x = oracle.logits(_parity.oracle_shape(inp), W.bits(inp.q), W.bits(inp.k_cache), bt,
+                      cut.numpy(), wl.scale)
+    _check_counts(counts, x)
+
+
+@pytest.mark.gpu
 def test_logit_histogram_rejects_bad_arguments():
     inp = W.generate(W.TINY)
     dev = _parity.DeviceInputs(inp)

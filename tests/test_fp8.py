@@ -140,11 +140,15 @@ def test_fp8_forced_fallback(_gpu, mode):
     phi, lo, hi = 0.0, -0.25, 0.25
     ref, ref_lse, ref_flag, margin = _parity.run_oracle(inp, phi=phi, lo=lo, hi=hi)
     assert ref_flag.all() and _parity.margin_ok(margin).all()
-    attn = binding.DecodeAttention(_parity.problem_for(inp, mode=mode, phi=phi, lo=lo, hi=hi), 0)
-    out, lse, flags, st = _parity.run_gpu(dev, want_stats=True, attn=attn)
-    _parity.compare(out, ref.reshape(out.shape), "bf16", where="fp8 forced fallback")
-    _parity.compare_lse(lse, ref_lse.reshape(lse.shape), where="fp8 forced fallback")
-    assert flags.cpu().numpy().all() and st.rows_flagged == 32
+    for sms in (0, 16):   # one KV head per group, then packed pairs (planned for 16 SMs)
+        attn = binding.DecodeAttention(
+            _parity.problem_for(inp, mode=mode, phi=phi, lo=lo, hi=hi, num_sms=sms), 0)
+        assert attn.info.kv_heads_per_group == (2 if sms else 1)
+        out, lse, flags, st = _parity.run_gpu(dev, want_stats=True, attn=attn)
+        where = f"fp8 forced fallback sms={sms}"
+        _parity.compare(out, ref.reshape(out.shape), "bf16", where=where)
+        _parity.compare_lse(lse, ref_lse.reshape(lse.shape), where=where)
+        assert flags.cpu().numpy().all() and st.rows_flagged == 32
 
 
 @pytest.mark.gpu
