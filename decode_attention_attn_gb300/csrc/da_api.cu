@@ -16,6 +16,7 @@
 #include <utility>
 
 #include "da_device.cuh"
+#include "da_mma.cuh"
 #include "da_scratch_cache.h"
 
 namespace da {
@@ -204,6 +205,229 @@ __global__ void __launch_bounds__(kHistThreads, G == 8 ? (sizeof(T) == 4 ? 3 : 2
     if (hist[i]) atomicAdd(&counts[i], (unsigned long long)hist[i]);
 }
 
+// ---- the histogram pass on the tensor cores (bf16 and FP8 caches) -------------------------
+// Persistent CTAs, two per SM where they fit: a producer warp TMA-loads each work item's K rows (128 tokens of one
+// sequence and KV head, as two 64-row halves laid out and swizzled as the split kernel's tiles)
+// and the group's q into a ring of stages; 8 consumer warps form S^T = K q^T for 8 rows of
+// each half with the split kernel's MMAs (mma_logits, mma_logits_fp8), so a row's G logits
+// cost a few MMA instructions instead of the CUDA-core pass's per-lane dot products and
+// butterflies. The producer looks up the next item's pages while the current one waits for its
+// stage; rows a bad block-table entry would have supplied are masked. Every wait is bounded: on
+// a timeout the CTA stops, having counted less.
+constexpr int kHmConsumerWarps = 8;
+constexpr int kHmThreads = (kHmConsumerWarps + 1) * 32;   // + one producer warp
+constexpr int kHmItemTokens = 2 * kStageTokens;            // 128: 16 rows per consumer warp
+constexpr int kHmMaxStages = 8;
+constexpr int kHmMaxBatchSmem = 4096;                      // lengths kept in shared memory
+
+struct HmLayout {
+  uint32_t bar_off, flag_off, lens_off, stage_off, stage_bytes, q_off, mask_off, total;
+};
+// es: K bytes per element; lens: sequence lengths held in shared memory
+__host__ __device__ inline HmLayout hm_layout(int D, int G, int es, int nbins, int stages,
+                                              int lens) {
+  HmLayout L;
+  L.bar_off = align_up((uint32_t)(nbins + 2) * 4u, 16);
+  L.flag_off = L.bar_off + 2u * stages * 8u;
+  L.lens_off = L.flag_off + 16u;
+  L.stage_off = align_up(L.lens_off + (uint32_t)lens * 4u, 1024);
+  L.q_off = (uint32_t)kHmItemTokens * D * es;
+  L.mask_off = L.q_off + align_up((uint32_t)G * D * 2u, 16);
+  L.stage_bytes = align_up(L.mask_off + 16u, 1024);
+  L.total = L.stage_off + (uint32_t)stages * L.stage_bytes + 1024;   // + aligning the base
+  return L;
+}
+
+// Bits [lo, hi) of a 64-bit word (both clamped to [0, 64]).
+__device__ __forceinline__ unsigned long long bit_range(int lo, int hi) {
+  lo = max(lo, 0);
+  hi = min(hi, 64);
+  if (hi <= lo) return 0ull;
+  const unsigned long long up = hi == 64 ? ~0ull : (1ull << hi) - 1ull;
+  return up & ~((1ull << lo) - 1ull);
+}
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kHmThreads, 2)
+    logit_histogram_mma_kernel(const __grid_constant__ Params p,
+                               const __grid_constant__ CUtensorMap tmk, float lo, float inv_w,
+                               int nbins, unsigned long long* __restrict__ counts, int stages) {
+  extern __shared__ uint8_t hm_raw[];
+  constexpr bool kFp8 = std::is_same<T, fp8e4m3>::value;
+  constexpr uint32_t kRowBytes = (uint32_t)D * sizeof(T);
+  constexpr uint32_t kQBytes = (uint32_t)G * D * 2u;   // bf16 q
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nlens = p.batch <= kHmMaxBatchSmem ? p.batch : 0;
+  const HmLayout L = hm_layout(D, G, sizeof(T), nbins, stages, nlens);
+  uint8_t* sm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(hm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  unsigned* hist = reinterpret_cast<unsigned*>(sm);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + L.bar_off);
+  uint64_t* empty = full + stages;
+  int& abort_flag = *reinterpret_cast<int*>(sm + L.flag_off);
+  int* lens = reinterpret_cast<int*>(sm + L.lens_off);
+  uint8_t* ring = sm + L.stage_off;
+
+  for (int i = tid; i < nbins + 2; i += kHmThreads) hist[i] = 0;
+  for (int i = tid; i < nlens; i += kHmThreads) {
+    const int raw = __ldg(p.seq_lens + i);
+    lens[i] = raw < 0 ? 0 : (raw > p.capacity ? p.capacity : raw);
+  }
+  if (tid == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kHmConsumerWarps);
+    }
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // Items it = (b * H_kv + kvh) * chunks + ch (fewer than 2^31, checked on the host); this
+  // CTA's are blockIdx.x, + gridDim.x, ...; next_item() skips those past their sequence's end.
+  const int chunks = (p.capacity + kHmItemTokens - 1) / kHmItemTokens;
+  const int items = p.batch * p.hkv * chunks;
+  auto seq_len = [&](int b) {
+    if (nlens) return lens[b];
+    const int raw = __ldg(p.seq_lens + b);
+    return raw < 0 ? 0 : (raw > p.capacity ? p.capacity : raw);
+  };
+  auto next_item = [&](int it) {
+    for (; it < items; it += gridDim.x)
+      if ((it % chunks) * kHmItemTokens < seq_len(it / chunks / p.hkv)) break;
+    return it < items ? it : items;
+  };
+  const uint32_t NS = (uint32_t)stages;
+  uint32_t k = 0;   // stages used so far (the same count in every warp)
+  if (warp == kHmConsumerWarps) {
+    const uint64_t pol = make_evict_first_policy();
+    const int box = p.box_tokens;
+    auto lookup = [&](int it) {   // the cache row of box `lane` of item it (-1: none or bad)
+      if (it >= items) return -1;
+      const int ch = it % chunks, b = it / chunks / p.hkv;
+      const int t0 = ch * kHmItemTokens, t1 = min(seq_len(b), t0 + kHmItemTokens);
+      const int t = t0 + lane * box;
+      if (t >= t1) return -1;
+      const int entry =
+          p.paged ? __ldg(p.block_table + (long long)b * p.max_blocks + t / p.page_size) : 0;
+      return token_row(p, b, t, entry);
+    };
+    uint32_t issued = 0;
+    int it = next_item(blockIdx.x);
+    int z = lookup(it);
+    while (it < items) {
+      const int nxt = next_item(it + gridDim.x);
+      const int z_next = lookup(nxt);   // in flight while this item waits for its stage
+      const int ch = it % chunks, kvh = (it / chunks) % p.hkv, b = it / chunks / p.hkv;
+      const int t0 = ch * kHmItemTokens, t1 = min(seq_len(b), t0 + kHmItemTokens);
+      const uint32_t slot = k % NS, ph = (k / NS) & 1u;
+      ++k;
+      bool stop = !mbar_wait(&empty[slot], ph ^ 1u, p.wait_limit_ns) ||
+                  *reinterpret_cast<volatile int*>(&abort_flag) != 0;
+      stop = __any_sync(0xffffffffu, stop);
+      if (stop) {
+        if (lane == 0) atomicExch(&abort_flag, 1);
+        break;
+      }
+      uint8_t* st = ring + slot * L.stage_bytes;
+      const int nbox = (t1 - t0 + box - 1) / box;   // lane i loads box i: rows [i box, (i+1) box)
+      const unsigned bad = __ballot_sync(0xffffffffu, lane < nbox && z < 0);
+      if (lane == 0) {
+        // the tile rows below t1, less the boxes of bad entries (rare)
+        unsigned long long m0 = bit_range(0, t1 - t0), m1 = bit_range(0, t1 - t0 - 64);
+        for (unsigned rest = bad; rest != 0u; rest &= rest - 1u) {
+          const int i = __ffs(rest) - 1;
+          m0 &= ~bit_range(i * box, (i + 1) * box);
+          m1 &= ~bit_range(i * box - 64, (i + 1) * box - 64);
+        }
+        reinterpret_cast<unsigned long long*>(st + L.mask_off)[0] = m0;
+        reinterpret_cast<unsigned long long*>(st + L.mask_off)[1] = m1;
+        mbar_arrive_expect_tx(&full[slot], (uint32_t)nbox * box * kRowBytes + kQBytes);
+        const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(p.q) +
+                                  ((long long)b * p.hq + (long long)kvh * G) * D;
+        bulk_load(st + L.q_off, qg, kQBytes, &full[slot]);
+      }
+      __syncwarp();
+      if (lane < nbox) {
+        // a bad entry reads past the pool (zero fill); its rows are masked
+        const int zz = z >= 0 ? z : p.num_blocks * p.page_size;
+        uint8_t* dst = st + (uint32_t)lane * box * kRowBytes;
+        if constexpr (kFp8)
+          tma_load_3d(dst, &tmk, &full[slot], 0, kvh, zz, pol);
+        else
+          tma_load_4d(dst, &tmk, &full[slot], 0, 0, kvh, zz, pol);
+      }
+      issued = k;
+      __syncwarp();
+      it = nxt;
+      z = z_next;
+    }
+    // never leave with copies in flight
+    if (lane == 0) {
+      const uint32_t first = issued > NS ? issued - NS : 0u;
+      for (uint32_t kk = first; kk < issued; ++kk)
+        mbar_wait(&full[kk % NS], (kk / NS) & 1u, p.wait_limit_ns);
+    }
+  } else {
+    // consumers: rows row0 .. row0 + 7 of each 64-row half, as a split-kernel warp
+    const int row0 = warp * kTokensPerWarp;
+    const std::conditional_t<kFp8, NoMmaLane, MmaLane<D>> ml(row0, lane);
+    const int hp = 2 * (lane & 3), tr = row0 + (lane >> 2);
+    for (int it = next_item(blockIdx.x); it < items; it = next_item(it + gridDim.x)) {
+      const uint32_t slot = k % NS, ph = (k / NS) & 1u;
+      ++k;
+      bool stop = !mbar_wait(&full[slot], ph, p.wait_limit_ns);
+      stop = __any_sync(0xffffffffu, stop);
+      if (stop) {
+        if (lane == 0) atomicExch(&abort_flag, 1);
+        break;
+      }
+      const uint8_t* st = ring + slot * L.stage_bytes;
+      const unsigned long long* mask =
+          reinterpret_cast<const unsigned long long*>(st + L.mask_off);
+      const uint32_t kt[2] = {smem_u32(st), smem_u32(st + kStageTokens * kRowBytes)};
+      MmaState<D, G> ms;
+      float sa[4], sb[4];
+      if constexpr (kFp8) {
+        mma_load_q_fp8<D, G>(p, ms, st + L.q_off, lane);   // qmul: the logit scale * 2^-s
+        mma_logits_fp8<D, G, 1>(ms, kt, row0, lane, sa, sb);
+      } else {
+        mma_load_q<D, G>(ms, st + L.q_off, lane);
+        ms.qmul = p.qscale;
+        mma_logits<D, G>(ms, ml, kt, sa, sb);
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {   // token tr of half c / 2, head hp + c % 2
+        const int h = hp + (c & 1);
+        const bool ok = h < G && ((mask[c >> 1] >> tr) & 1ull);
+        if (ok) atomicAdd(&hist[hist_bin((sa[c] + sb[c]) * ms.qmul, lo, inv_w, nbins)], 1u);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < nbins + 2; i += kHmThreads)
+    if (hist[i]) atomicAdd(&counts[i], (unsigned long long)hist[i]);
+}
+
+template <typename T, int D>
+const void* histogram_mma_kernel_for_d(int G) {
+  switch (G) {
+    case 1: return reinterpret_cast<const void*>(&logit_histogram_mma_kernel<T, D, 1>);
+    case 2: return reinterpret_cast<const void*>(&logit_histogram_mma_kernel<T, D, 2>);
+    case 4: return reinterpret_cast<const void*>(&logit_histogram_mma_kernel<T, D, 4>);
+    case 8: return reinterpret_cast<const void*>(&logit_histogram_mma_kernel<T, D, 8>);
+    default: return nullptr;
+  }
+}
+
+template <typename T>
+const void* histogram_mma_kernel_for(int D, int G) {
+  return D == 64 ? histogram_mma_kernel_for_d<T, 64>(G)
+                 : (D == 128 ? histogram_mma_kernel_for_d<T, 128>(G) : nullptr);
+}
+
 template <typename T, int D>
 const void* histogram_kernel_for_d(int G) {
   switch (G) {
@@ -362,7 +586,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // bf16 tensor-core kernels read the tile with ldmatrix and need the 128-byte swizzle, whose
 // rows are at most 128 bytes: for them the view is 4-D, [tokens, Hkv, D / 64, 64]. FP8 tiles
 // keep the 3-D view (a row of D = 64 or 128 bytes), 128-byte-swizzled when D = 128.
-int make_kv_map(const da_plan& pl, const void* base, bool swizzled, CUtensorMap* map) {
+int make_kv_map(const da_plan& pl, const void* base, bool swizzled, int hp,
+                CUtensorMap* map) {
   auto fn = encode_fn();
   if (!fn) {
     g_cuda_error = "cuTensorMapEncodeTiled is not available from the driver";
@@ -375,8 +600,8 @@ int make_kv_map(const da_plan& pl, const void* base, bool swizzled, CUtensorMap*
   const int es = pl.kv_es;
   const cuuint64_t strides[2] = {(cuuint64_t)p.head_dim * es,
                                  (cuuint64_t)p.num_kv_heads * p.head_dim * es};
-  // a box holds the rows of the split kernel's hp KV heads of box_tokens tokens
-  const cuuint32_t box[3] = {(cuuint32_t)p.head_dim, (cuuint32_t)pl.hp, (cuuint32_t)pl.box_tokens};
+  // a box holds the rows of hp KV heads (a split-kernel group) of box_tokens tokens
+  const cuuint32_t box[3] = {(cuuint32_t)p.head_dim, (cuuint32_t)hp, (cuuint32_t)pl.box_tokens};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   // L2 fills no wider than a KV row: with a wider promotion every box row also pulls in the
   // neighbouring head's row, which a paged gather seldom reads before it is evicted (FP8 rows
@@ -750,8 +975,8 @@ int decode_attn_run_ex(const da_plan* plan, const da_run_args* args) {
   // tensor-core kernels (both modes, so the recompute pass too) read 128-byte-swizzled tiles
   const bool mma = uses_mma(pl.kv_es, p.qkv_dtype == DA_F16, pl.sgroup);
   CUtensorMap tmk, tmv;
-  int rc = make_kv_map(pl, k_cache, mma, &tmk);
-  if (rc == DA_OK) rc = make_kv_map(pl, v_cache, mma, &tmv);
+  int rc = make_kv_map(pl, k_cache, mma, pl.hp, &tmk);
+  if (rc == DA_OK) rc = make_kv_map(pl, v_cache, mma, pl.hp, &tmv);
   if (rc != DA_OK) return rc;
 
   Params kp;
@@ -895,6 +1120,55 @@ int decode_attn_logit_histogram(const da_plan* plan, const void* q, const void* 
   const float inv_w = (float)((double)nbins / ((double)hi - (double)lo));
   if (!std::isfinite(inv_w) || !(inv_w > 0.f)) return DA_ERR_INVALID_ARG;
 
+  // an FP8 cache's codes stand for code * k_scale: fold it into the logit scale
+  float xscale = pl.prob.kv_fp8 ? (float)((double)scale * (double)pl.prob.k_scale) : scale;
+  const int D = pl.prob.head_dim, G = pl.group;
+  if (pl.prob.kv_fp8 || pl.prob.qkv_dtype == DA_BF16) {
+    // bf16 and FP8 caches: the tensor-core pass
+    const void* fn = pl.prob.kv_fp8 ? histogram_mma_kernel_for<fp8e4m3>(D, G)
+                                    : histogram_mma_kernel_for<__nv_bfloat16>(D, G);
+    if (!fn) return DA_ERR_UNSUPPORTED;
+    const long long items = (long long)pl.prob.batch * pl.prob.num_kv_heads *
+                            ((pl.capacity + kHmItemTokens - 1) / kHmItemTokens);
+    if (items >= (1ll << 31) - pl.num_sms) return DA_ERR_UNSUPPORTED;   // 32-bit item indices
+    const int nlens = pl.prob.batch <= kHmMaxBatchSmem ? pl.prob.batch : 0;
+    // Two CTAs per SM (each with the deepest ring that then fits) where both fit: a CTA turns
+    // its items around one at a time, so two of them keep more of each SM busy than one
+    // deeper ring.
+    constexpr size_t kSmSmem = 233472, kBlockReserve = 1024;   // per SM; reserved per CTA
+    int stages = 0, per_sm = 1;
+    size_t smem = 0;
+    for (int target = 2; target >= 1 && stages == 0; --target)
+      for (int st = kHmMaxStages; st >= 2 && stages == 0; --st) {
+        const size_t bytes = hm_layout(D, G, pl.kv_es, nbins, st, nlens).total;
+        if (bytes <= kSmemLimit && (size_t)target * (bytes + kBlockReserve) <= kSmSmem) {
+          stages = st;
+          smem = bytes;
+          per_sm = target;
+        }
+      }
+    if (stages == 0) return DA_ERR_UNSUPPORTED;
+    cudaError_t e =
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(histogram smem)");
+    int fit = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, fn, kHmThreads, smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    per_sm = std::max(1, std::min(per_sm, fit));
+    CUtensorMap tmk;   // the split kernel's tiles of one KV head
+    const int rc = make_kv_map(pl, k_cache, true, 1, &tmk);
+    if (rc != DA_OK) return rc;
+    Params kp;
+    fill_common(pl, kp, block_table, seq_lens, nullptr);
+    kp.q = q;
+    kp.qscale = xscale;
+    const int grid = (int)std::max(1ll, std::min(items, (long long)pl.num_sms * per_sm));
+    void* args[7] = {&kp, &tmk, &lo, const_cast<float*>(&inv_w), &nbins, &counts, &stages};
+    e = cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(kHmThreads), args, smem,
+                         static_cast<cudaStream_t>(cuda_stream));
+    return e == cudaSuccess ? DA_OK : cuda_fail(e, "launching the logit histogram kernel");
+  }
+
   const void* fn = nullptr;
   if (pl.prob.kv_fp8) fn = histogram_kernel_for<fp8e4m3>(pl.prob.head_dim, pl.group);
   else switch (pl.prob.qkv_dtype) {
@@ -919,8 +1193,6 @@ int decode_attn_logit_histogram(const da_plan* plan, const void* q, const void* 
   Params kp;
   fill_common(pl, kp, block_table, seq_lens, nullptr);
   kp.q = q;
-  // an FP8 cache's codes stand for code * k_scale: fold it into the logit scale
-  float xscale = pl.prob.kv_fp8 ? (float)((double)scale * (double)pl.prob.k_scale) : scale;
   void* args[7] = {&kp, &k_cache, &xscale, &lo, const_cast<float*>(&inv_w), &nbins, &counts};
   e = cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(kHistThreads), args, smem,
                        static_cast<cudaStream_t>(cuda_stream));

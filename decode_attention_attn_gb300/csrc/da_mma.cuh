@@ -359,16 +359,18 @@ __device__ __forceinline__ void v_masks(const int (&n)[2], int row0, int lane, u
 // kt / vt: shared-memory addresses of the K and V tiles of stages 0 and 1 (with n[1] == 0 there
 // is no second stage: the caller passes stage 0's tiles again and every stage-1 token is
 // masked, so no stale shared memory enters the MMA).
-template <int D, int G, bool UNIFIED, bool LOCAL>
-__device__ __forceinline__ void mma_consume(const Params& p, MmaState<D, G>& st,
-                                            const MmaLane<D>& ml, const uint32_t (&kt)[2],
-                                            const uint32_t (&vt)[2], const int (&n)[2], int row0,
-                                            int lane, uint32_t& fmask) {
+// S^T = K q^T over the warp's 8 rows of two stages of bf16 tiles (kt as in mma_consume), as
+// two accumulator chains (even and odd k-steps, which halves the dependent latency): the
+// logits are sa + sb in the C-fragment layout (token lane/4 of stage 0 in [0], [1], of stage
+// 1 in [2], [3]; heads 2 (lane % 4) and that + 1).
+template <int D, int G>
+__device__ __forceinline__ void mma_logits(const MmaState<D, G>& st, const MmaLane<D>& ml,
+                                           const uint32_t (&kt)[2], float (&sa)[4],
+                                           float (&sb)[4]) {
   constexpr int KS = MmaState<D, G>::KS;
-  const uint32_t kbase = ml.kst ? kt[1] : kt[0], vbase = ml.vst ? vt[1] : vt[0];
-
-  // S^T = K q^T: two accumulator chains (even and odd k-steps) halve the dependent latency
-  float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+  const uint32_t kbase = ml.kst ? kt[1] : kt[0];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) sa[i] = sb[i] = 0.f;
 #pragma unroll
   for (int kk = 0; kk < KS; ++kk) {
     uint32_t a0, a1, a2, a3;
@@ -378,6 +380,18 @@ __device__ __forceinline__ void mma_consume(const Params& p, MmaState<D, G>& st,
     else
       mma_bf16(sa, a0, a1, a2, a3, st.qb[kk][0], st.qb[kk][1]);
   }
+}
+
+template <int D, int G, bool UNIFIED, bool LOCAL>
+__device__ __forceinline__ void mma_consume(const Params& p, MmaState<D, G>& st,
+                                            const MmaLane<D>& ml, const uint32_t (&kt)[2],
+                                            const uint32_t (&vt)[2], const int (&n)[2], int row0,
+                                            int lane, uint32_t& fmask) {
+  constexpr int KS = MmaState<D, G>::KS;
+  const uint32_t vbase = ml.vst ? vt[1] : vt[0];
+
+  float sa[4], sb[4];
+  mma_logits<D, G>(st, ml, kt, sa, sb);
   uint32_t bh0, bh1, bl0, bl1, vm0, vm1;
   float f0, f1;
   mma_softmax<D, G, UNIFIED, LOCAL, false>(p, st, sa, sb, n, row0, lane, fmask, bh0, bh1, bl0,
@@ -456,27 +470,21 @@ __device__ __forceinline__ void mma_load_q_fp8(const Params& p, MmaState<D, G>& 
   st.qmul = p.qscale * down;
 }
 
-// mma_consume over FP8 tiles (kt / vt, n, row0 as there). HP > 1: the tiles hold HP KV heads'
-// rows of every token (row t * HP + h) and the group's G columns are HP blocks of G / HP query
-// heads, one block per KV head. Each contraction then runs once per KV head with the other
-// heads' columns of its B operand zeroed, so that all of them add into the same accumulators:
-// S^T = sum_h K_h [q^T, head h's columns], O^T += sum_h V_h^T [P^T, head h's columns]. The
-// MMA's 8 columns are then all in use, where an unpacked group of 4 heads leaves half of them
-// (and of the softmax work) idle.
-template <int D, int G, int HP, bool UNIFIED, bool LOCAL>
-__device__ __forceinline__ void mma_consume_fp8(const Params& p, MmaState<D, G>& st,
-                                                const uint32_t (&kt)[2], const uint32_t (&vt)[2],
-                                                const int (&n)[2], int row0, int lane,
-                                                uint32_t& fmask) {
+// S^T = K q^T over FP8 tiles (kt, row0 as in mma_consume; HP KV heads per token row, as in
+// mma_consume_fp8 below), into two accumulator chains shared by the KV heads: the logits are
+// sa + sb, laid out as mma_logits leaves them.
+template <int D, int G, int HP>
+__device__ __forceinline__ void mma_logits_fp8(const MmaState<D, G>& st, const uint32_t (&kt)[2],
+                                               int row0, int lane, float (&sa)[4],
+                                               float (&sb)[4]) {
   static_assert(G % HP == 0, "every KV head has the same number of query heads");
   constexpr int KS = MmaState<D, G>::KS;
   constexpr int KW = D / 16;   // 4-byte words of a lane's K bytes (one per k-step)
   const int g = lane >> 2, c = lane & 3;
   const int bh = g / (G / HP);   // KV head of this lane's B column (query head g)
-
-  // S^T = K q^T: A rows 0-7 = token row0 + g of stage 0, rows 8-15 = the same of stage 1;
-  // two accumulator chains (even and odd k-steps), shared by the KV heads
-  float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+  // A rows 0-7 = token row0 + g of stage 0, rows 8-15 = the same of stage 1
+#pragma unroll
+  for (int i = 0; i < 4; ++i) sa[i] = sb[i] = 0.f;
 #pragma unroll
   for (int h = 0; h < HP; ++h) {
     uint32_t k0[KW], k1[KW];
@@ -498,6 +506,25 @@ __device__ __forceinline__ void mma_consume_fp8(const Params& p, MmaState<D, G>&
               on ? st.qb[kk][1] : 0u);
     }
   }
+}
+
+// mma_consume over FP8 tiles (kt / vt, n, row0 as there). HP > 1: the tiles hold HP KV heads'
+// rows of every token (row t * HP + h) and the group's G columns are HP blocks of G / HP query
+// heads, one block per KV head. Each contraction then runs once per KV head with the other
+// heads' columns of its B operand zeroed, so that all of them add into the same accumulators:
+// S^T = sum_h K_h [q^T, head h's columns], O^T += sum_h V_h^T [P^T, head h's columns]. The
+// MMA's 8 columns are then all in use, where an unpacked group of 4 heads leaves half of them
+// (and of the softmax work) idle.
+template <int D, int G, int HP, bool UNIFIED, bool LOCAL>
+__device__ __forceinline__ void mma_consume_fp8(const Params& p, MmaState<D, G>& st,
+                                                const uint32_t (&kt)[2], const uint32_t (&vt)[2],
+                                                const int (&n)[2], int row0, int lane,
+                                                uint32_t& fmask) {
+  constexpr int KS = MmaState<D, G>::KS;
+  const int g = lane >> 2, c = lane & 3;
+  const int bh = g / (G / HP);   // KV head of this lane's B column (query head g)
+  float sa[4], sb[4];
+  mma_logits_fp8<D, G, HP>(st, kt, row0, lane, sa, sb);
   uint32_t bh0, bh1, bl0, bl1, vm0, vm1;
   float f0, f1;
   mma_softmax<D, G, UNIFIED, LOCAL, true>(p, st, sa, sb, n, row0, lane, fmask, bh0, bh1, bl0,
