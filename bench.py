@@ -701,7 +701,9 @@ def run_histogram(args):
                    "l2": f"flushed before every timed step: {FLUSH_BYTES >> 20} MiB written, then {FLUSH_BYTES >> 20} MiB of another buffer read"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "peak_source": f"{peak_kind} hbm_gbs", "kernel": "logit_histogram_kernel",
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "kernel": ("logit_histogram_mma_kernel"
+                                if wl.kv_storage in ("bf16", "e4m3") else "logit_histogram_kernel"),
                      "traffic": profiled_traffic(wl.name, "logit_histogram")},
         "clocks": clocks,
         "gpu_launches": args.steps,
