@@ -1,6 +1,7 @@
 // da_api.cu -- host side of the C ABI declared in include/decode_attn.h: problem validation,
 // the launch plan (split policy, grid, pipeline depth, workspace layout), TMA tensor maps,
-// kernel launches, error reporting and the debug gather hook.
+// kernel launches, error reporting and the debug gather hook; and the logit-histogram kernels
+// of the phi calibration pass.
 #include "decode_attn.h"
 
 #include <cudaTypedefs.h>

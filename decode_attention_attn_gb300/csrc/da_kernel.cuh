@@ -1,7 +1,8 @@
 // da_kernel.cuh -- the split-KV decode-attention kernel for sm_103a.
 //
 // One persistent CTA per SM walks a list of "pieces": (sequence b, KV head kvh, token
-// range [t0, t1)). A piece is one Flash-Decoding split ("Flash-Decoding: Mathematical
+// range [t0, t1)); for an FP8 cache packed in pairs, kvh names a pair of KV heads (Cfg::kHp).
+// A piece is one Flash-Decoding split ("Flash-Decoding: Mathematical
 // Foundations, ...", "Mathematical Formulation of Split-KV Parallelism"): it yields the
 // partial output O, the maximum m and the sum l for all G query heads of its KV head at
 // once, so each KV row is read from HBM once for the whole group ("FlashAttention and
