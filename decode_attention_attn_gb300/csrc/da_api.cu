@@ -207,17 +207,19 @@ __global__ void __launch_bounds__(kHistThreads, G == 8 ? (sizeof(T) == 4 ? 3 : 2
 }
 
 // ---- the histogram pass on the tensor cores (bf16 and FP8 caches) -------------------------
-// Persistent CTAs, two per SM where they fit: a producer warp TMA-loads each work item's K rows (128 tokens of one
-// sequence and KV head, as two 64-row halves laid out and swizzled as the split kernel's tiles)
-// and the group's q into a ring of stages; 8 consumer warps form S^T = K q^T for 8 rows of
-// each half with the split kernel's MMAs (mma_logits, mma_logits_fp8), so a row's G logits
+// Persistent CTAs, up to four per SM: a producer warp TMA-loads each work item's K rows (64
+// tokens of one sequence and KV head, laid out and swizzled as the split kernel's tiles) and
+// the group's q into a ring of stages; 4 consumer warps form S^T = K q^T for 8 rows of each
+// 32-row half with the split kernel's MMAs (mma_logits, mma_logits_fp8), so a row's G logits
 // cost a few MMA instructions instead of the CUDA-core pass's per-lane dot products and
 // butterflies. The producer looks up the next item's pages while the current one waits for its
 // stage; rows a bad block-table entry would have supplied are masked. Every wait is bounded: on
 // a timeout the CTA stops, having counted less.
-constexpr int kHmConsumerWarps = 8;
+constexpr int kHmConsumerWarps = 4;
 constexpr int kHmThreads = (kHmConsumerWarps + 1) * 32;   // + one producer warp
-constexpr int kHmItemTokens = 2 * kStageTokens;            // 128: 16 rows per consumer warp
+// an item: two halves of 8 rows per consumer warp, 16 rows = one MMA's tokens per warp
+constexpr int kHmHalfTokens = kHmConsumerWarps * kTokensPerWarp;   // 32
+constexpr int kHmItemTokens = 2 * kHmHalfTokens;                    // 64
 constexpr int kHmMaxStages = 8;
 constexpr int kHmMaxBatchSmem = 4096;                      // lengths kept in shared memory
 
@@ -249,7 +251,7 @@ __device__ __forceinline__ unsigned long long bit_range(int lo, int hi) {
 }
 
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(kHmThreads, 2)
+__global__ void __launch_bounds__(kHmThreads, 4)
     logit_histogram_mma_kernel(const __grid_constant__ Params p,
                                const __grid_constant__ CUtensorMap tmk, float lo, float inv_w,
                                int nbins, unsigned long long* __restrict__ counts, int stages) {
@@ -386,7 +388,7 @@ __global__ void __launch_bounds__(kHmThreads, 2)
       const uint8_t* st = ring + slot * L.stage_bytes;
       const unsigned long long* mask =
           reinterpret_cast<const unsigned long long*>(st + L.mask_off);
-      const uint32_t kt[2] = {smem_u32(st), smem_u32(st + kStageTokens * kRowBytes)};
+      const uint32_t kt[2] = {smem_u32(st), smem_u32(st + kHmHalfTokens * kRowBytes)};
       MmaState<D, G> ms;
       float sa[4], sb[4];
       if constexpr (kFp8) {
@@ -400,7 +402,8 @@ __global__ void __launch_bounds__(kHmThreads, 2)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {   // token tr of half c / 2, head hp + c % 2
         const int h = hp + (c & 1);
-        const bool ok = h < G && ((mask[c >> 1] >> tr) & 1ull);
+        const int row = (c >> 1) * kHmHalfTokens + tr;   // tile row
+        const bool ok = h < G && ((mask[row >> 6] >> (row & 63)) & 1ull);
         if (ok) atomicAdd(&hist[hist_bin((sa[c] + sb[c]) * ms.qmul, lo, inv_w, nbins)], 1u);
       }
       __syncwarp();
@@ -1133,13 +1136,13 @@ int decode_attn_logit_histogram(const da_plan* plan, const void* q, const void* 
                             ((pl.capacity + kHmItemTokens - 1) / kHmItemTokens);
     if (items >= (1ll << 31) - pl.num_sms) return DA_ERR_UNSUPPORTED;   // 32-bit item indices
     const int nlens = pl.prob.batch <= kHmMaxBatchSmem ? pl.prob.batch : 0;
-    // Two CTAs per SM (each with the deepest ring that then fits) where both fit: a CTA turns
-    // its items around one at a time, so two of them keep more of each SM busy than one
-    // deeper ring.
+    // As many CTAs per SM as fit, up to 4, each with the deepest ring that then fits: a CTA
+    // turns its items around one at a time, so several of them keep more of each SM busy than
+    // one deeper ring.
     constexpr size_t kSmSmem = 233472, kBlockReserve = 1024;   // per SM; reserved per CTA
     int stages = 0, per_sm = 1;
     size_t smem = 0;
-    for (int target = 2; target >= 1 && stages == 0; --target)
+    for (int target = 4; target >= 1 && stages == 0; --target)
       for (int st = kHmMaxStages; st >= 2 && stages == 0; --st) {
         const size_t bytes = hm_layout(D, G, pl.kv_es, nbins, st, nlens).total;
         if (bytes <= kSmemLimit && (size_t)target * (bytes + kBlockReserve) <= kSmSmem) {
