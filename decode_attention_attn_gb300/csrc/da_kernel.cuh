@@ -962,7 +962,6 @@ __device__ __forceinline__ void run_consumers_mma(const Params& p, Sched s, uint
       for (int i = 0; i < 4; ++i) st.o[j][i] = 0.f;
     st.den[0] = st.den[1] = 0.f;
     st.m[0] = st.m[1] = -INFINITY;
-    st.mt[0] = st.mt[1] = -INFINITY;
     st.sw = false;
     st.qmul = p.qscale;   // FP8 tiles: reset with q's scale when q is loaded
     uint32_t fmask = 0;
@@ -1006,7 +1005,9 @@ __device__ __forceinline__ void run_consumers_mma(const Params& p, Sched s, uint
       }
       k += pair ? 2u : 1u;
     }
-    const bool at_phi = UNIFIED && !(LOCAL && st.sw);   // the state is relative to phi
+    // the state is relative to phi (bf16 tiles, unified phase) or to st.m (FP8 tiles, whose
+    // unified phase keeps its own power-of-two reference there)
+    const bool at_phi = UNIFIED && !kFp8 && !(LOCAL && st.sw);
     publish_mma<T, D, G>(st, at_phi ? p.phi2 : st.m[0], at_phi ? p.phi2 : st.m[1], fmask, mm, ml,
                          mflag, wbuf, warp, lane);
     combine_piece<T, D, G>(p, pc, s.first_phase, mm, ml, mflag, wbuf, misc, warp, lane, ctid);

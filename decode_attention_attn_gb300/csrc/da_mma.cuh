@@ -165,8 +165,7 @@ struct MmaState {
                                         // (FP8 tiles: d = (D/8)(lane / 4) + 2 mt, d' = d + 1)
   float den[2];                         // this lane's share of heads hp, hp + 1 denominators
   float m[2];                           // synchronised recurrence: their running maxima
-  float mt[2];                          // split-local fallback, before the switch: the lane's
-                                        // maximum logit of each head so far
+                                        // (FP8 tiles, unified phase: the reference r)
   float qmul;                           // logit factor: scale * log2 e (FP8 tiles: times 2^-s,
                                         // s the power of two q was scaled by)
   bool sw;                              // split-local fallback: the warp has switched to the
@@ -190,16 +189,18 @@ __device__ __forceinline__ void mma_load_q(MmaState<D, G>& st, const uint8_t* qs
 // two S^T accumulator chains sa, sb (token lane/4 of stage 0 in [0], [1], of stage 1 in
 // [2], [3]; heads hp, hp + 1), the range check, the running maxima of the synchronised
 // recurrence, p, the denominators, and P^T as hi / lo B fragments (bh*, bl*): bf16, or f16
-// when F16. f16 holds only p <= 2^15 and loses p below 2^-24, so in the unified phase (p
-// relative to phi, of any size) the F16 step takes each head's p relative to the stage pair's
-// own maximum m_t and returns f = 2^(m_t - phi) per head (f0, f1): the caller adds the pair's
-// P . V to the accumulators times f, which is the same sum. f0 = f1 = 1 otherwise.
+// when F16. f16 holds only p <= 2^15 and keeps 11 bits only above 2^-14, so in the unified
+// phase the F16 step takes p = 2^(x - r) against a reference r = phi + 16 k per head and warp,
+// with k the smallest integer that puts the largest logit so far in (r - 1, r + 15]. k starts
+// from the first logits and only grows, in steps that rescale the state by 2^-16 each, so p
+// stays exactly the unified 2^(x - phi) up to one power of two per warp and head, and no stage
+// pair is rescaled on its own. The state is then relative to r (kept in st.m), not to phi.
 template <int D, int G, bool UNIFIED, bool LOCAL, bool F16>
 __device__ __forceinline__ void mma_softmax(const Params& p, MmaState<D, G>& st,
                                             const float (&sa)[4], const float (&sb)[4],
                                             const int (&n)[2], int row0, int lane,
                                             uint32_t& fmask, uint32_t& bh0, uint32_t& bh1,
-                                            uint32_t& bl0, uint32_t& bl1, float& f0, float& f1) {
+                                            uint32_t& bl0, uint32_t& bl1) {
   constexpr int KS = MmaState<D, G>::KS;
   // The lane's logits: [0], [1] = token lane/4 of stage 0 for heads hp, hp + 1; [2], [3] = the
   // same row of stage 1. A head's 16 logits sit in the 8 lanes that share lane % 4.
@@ -220,40 +221,27 @@ __device__ __forceinline__ void mma_softmax(const Params& p, MmaState<D, G>& st,
     if (!st.sw) {
       bool out = false;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if (valid[c]) {
-          out = out || x[c] < p.lo2 || x[c] > p.hi2;
-          if constexpr (F16) st.mt[c & 1] = fmaxf(st.mt[c & 1], x[c]);
-        }
-      }
-      if (__any_sync(0xffffffffu, out)) {
-        // The new reference must bound every logit so far from above. f16 P (FP8 tiles) needs
-        // the maximum itself, kept per lane. With bf16 P a bound within log2(tokens) of it is
-        // as good, and the state gives one for free: its denominators are sums of 2^(x - phi)
-        // over in-range logits, so phi + log2(sum) lies between the maximum and the maximum
-        // plus log2 of the warp's token count.
-        float m0, m1;
-        if constexpr (F16) {
-          m0 = st.mt[0];
-          m1 = st.mt[1];
-        } else {
-          m0 = st.den[0];
-          m1 = st.den[1];
-        }
+      for (int c = 0; c < 4; ++c)
+        if (valid[c]) out = out || x[c] < p.lo2 || x[c] > p.hi2;
+      if constexpr (F16) {
+        // f16 P: the state is already relative to the warp's reference r = st.m, which lies
+        // within 15 below the largest logit so far at most; the synchronised recurrence
+        // continues from it
+        if (__any_sync(0xffffffffu, out)) st.sw = true;
+      } else if (__any_sync(0xffffffffu, out)) {
+        // The new reference must bound every logit so far from above. With bf16 P a bound
+        // within log2(tokens) of the maximum is as good as the maximum, and the state gives
+        // one for free: its denominators are sums of 2^(x - phi) over in-range logits, so
+        // phi + log2(sum) lies between the maximum and the maximum plus log2 of the warp's
+        // token count.
+        float m0 = st.den[0], m1 = st.den[1];
 #pragma unroll
         for (int o = 4; o <= 16; o <<= 1) {
-          if constexpr (F16) {
-            m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
-            m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
-          } else {
-            m0 += __shfl_xor_sync(0xffffffffu, m0, o);
-            m1 += __shfl_xor_sync(0xffffffffu, m1, o);
-          }
+          m0 += __shfl_xor_sync(0xffffffffu, m0, o);
+          m1 += __shfl_xor_sync(0xffffffffu, m1, o);
         }
-        if constexpr (!F16) {
-          m0 = m0 > 0.f ? p.phi2 + fast_log2(m0) : -INFINITY;
-          m1 = m1 > 0.f ? p.phi2 + fast_log2(m1) : -INFINITY;
-        }
+        m0 = m0 > 0.f ? p.phi2 + fast_log2(m0) : -INFINITY;
+        m1 = m1 > 0.f ? p.phi2 + fast_log2(m1) : -INFINITY;
         const float al0 = m0 > -INFINITY ? fast_exp2(p.phi2 - m0) : 1.f;
         const float al1 = m1 > -INFINITY ? fast_exp2(p.phi2 - m1) : 1.f;
 #pragma unroll
@@ -298,7 +286,8 @@ __device__ __forceinline__ void mma_softmax(const Params& p, MmaState<D, G>& st,
     ref0 = st.m[0];   // -inf only while all of the head's tokens so far are masked
     ref1 = st.m[1];
   } else if constexpr (F16) {
-    // unified phase, f16 P: each head's p relative to its maximum over this stage pair
+    // unified phase, f16 P: the reference r = phi + 16 k (see above), raised when this stage
+    // pair's largest logit passes r + 15
     float m0 = fmaxf(valid[0] ? x[0] : -INFINITY, valid[2] ? x[2] : -INFINITY);
     float m1 = fmaxf(valid[1] ? x[1] : -INFINITY, valid[3] ? x[3] : -INFINITY);
 #pragma unroll
@@ -306,20 +295,36 @@ __device__ __forceinline__ void mma_softmax(const Params& p, MmaState<D, G>& st,
       m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
       m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
     }
-    ref0 = m0 > -INFINITY ? m0 : p.phi2;
-    ref1 = m1 > -INFINITY ? m1 : p.phi2;
-    f0 = m0 > -INFINITY ? fast_exp2(m0 - p.phi2) : 0.f;
-    f1 = m1 > -INFINITY ? fast_exp2(m1 - p.phi2) : 0.f;
+    const bool up0 = m0 > -INFINITY && !(m0 <= st.m[0] + 15.f);   // also when r is still -inf
+    const bool up1 = m1 > -INFINITY && !(m1 <= st.m[1] + 15.f);
+    if (__any_sync(0xffffffffu, up0 || up1)) {
+      const float r0 = up0 ? p.phi2 + 16.f * ceilf((m0 - p.phi2 - 15.f) * 0.0625f) : st.m[0];
+      const float r1 = up1 ? p.phi2 + 16.f * ceilf((m1 - p.phi2 - 15.f) * 0.0625f) : st.m[1];
+      const float al0 = up0 && st.m[0] > -INFINITY ? fast_exp2(st.m[0] - r0) : 1.f;
+      const float al1 = up1 && st.m[1] > -INFINITY ? fast_exp2(st.m[1] - r1) : 1.f;
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        st.o[mt][0] *= al0;
+        st.o[mt][1] *= al1;
+        st.o[mt][2] *= al0;
+        st.o[mt][3] *= al1;
+      }
+      st.den[0] *= al0;
+      st.den[1] *= al1;
+      st.m[0] = r0;
+      st.m[1] = r1;
+    }
+    ref0 = st.m[0];   // -inf only while all of the head's tokens so far are masked
+    ref1 = st.m[1];
   }
   float pr[4];
-  if (!F16 || !UNIFIED || (LOCAL && st.sw)) f0 = f1 = 1.f;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     pr[c] = valid[c] ? fast_exp2(x[c] - ((c & 1) ? ref1 : ref0)) : 0.f;
     if (UNIFIED && valid[c] && (x[c] < p.lo2 || x[c] > p.hi2)) fmask |= 1u << (hp + (c & 1));
   }
-  st.den[0] += f0 * (pr[0] + pr[2]);
-  st.den[1] += f1 * (pr[1] + pr[3]);
+  st.den[0] += pr[0] + pr[2];
+  st.den[1] += pr[1] + pr[3];
 
   // P as hi + lo (lower half = head hp), transposed into B fragments of P^T:
   // b0 = stage-0 tokens 2 (lane % 4), +1 of head lane / 4, b1 = the same of stage 1
@@ -393,9 +398,8 @@ __device__ __forceinline__ void mma_consume(const Params& p, MmaState<D, G>& st,
   float sa[4], sb[4];
   mma_logits<D, G>(st, ml, kt, sa, sb);
   uint32_t bh0, bh1, bl0, bl1, vm0, vm1;
-  float f0, f1;
   mma_softmax<D, G, UNIFIED, LOCAL, false>(p, st, sa, sb, n, row0, lane, fmask, bh0, bh1, bl0,
-                                           bl1, f0, f1);
+                                           bl1);
   v_masks(n, row0, lane, vm0, vm1);
 
   // O^T += V^T P^T: per m-tile of 16 d, A fragments (d 0-7 | 8-15) x (stage-0 | stage-1 tokens)
@@ -526,10 +530,8 @@ __device__ __forceinline__ void mma_consume_fp8(const Params& p, MmaState<D, G>&
   float sa[4], sb[4];
   mma_logits_fp8<D, G, HP>(st, kt, row0, lane, sa, sb);
   uint32_t bh0, bh1, bl0, bl1, vm0, vm1;
-  float f0, f1;
   mma_softmax<D, G, UNIFIED, LOCAL, true>(p, st, sa, sb, n, row0, lane, fmask, bh0, bh1, bl0,
-                                          bl1, f0, f1);
-  const bool scaled = UNIFIED && !(LOCAL && st.sw);   // the unified phase: P . V times f
+                                          bl1);
   v_masks(n, row0, lane, vm0, vm1);
   const bool tail = (vm0 & vm1) != 0xffffffffu;
 
@@ -559,45 +561,28 @@ __device__ __forceinline__ void mma_consume_fp8(const Params& p, MmaState<D, G>&
       vd[h][0] = u.x; vd[h][1] = u.y;
     }
   }
-  // the unified phase scales each stage pair's P . V by f into the accumulators; the branch is
-  // taken once per stage pair, outside the m-tile loop
-  auto pv = [&](auto scaled_tag) {
-    constexpr bool SC = decltype(scaled_tag)::value;
 #pragma unroll
-    for (int mt = 0; mt < KS; ++mt) {
-      // bytes [token 2c, token 2c + 1] of d (the lower half) and of d + 1 (the upper half)
-      const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
-      float t4[4] = {0.f, 0.f, 0.f, 0.f};
-      float (&acc)[4] = SC ? t4 : st.o[mt];
+  for (int mt = 0; mt < KS; ++mt) {
+    // bytes [token 2c, token 2c + 1] of d (the lower half) and of d + 1 (the upper half)
+    const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
 #pragma unroll
-      for (int h = 0; h < HP; ++h) {
-        const uint32_t x0 = prmt(va[h][mt >> 1], vb[h][mt >> 1], sel);
-        const uint32_t x1 = prmt(vc[h][mt >> 1], vd[h][mt >> 1], sel);
-        uint32_t a0, a1, a2, a3;
-        e4m3x4_to_f16x2(x0, a0, a1);
-        e4m3x4_to_f16x2(x1, a2, a3);
-        if (tail) {
-          a0 &= vm0;
-          a1 &= vm0;
-          a2 &= vm1;
-          a3 &= vm1;
-        }
-        const uint32_t pm = HP == 1 || bh == h ? 0xffffffffu : 0u;   // this head's columns
-        mma_f16(acc, a0, a1, a2, a3, bh0 & pm, bh1 & pm);
-        mma_f16(acc, a0, a1, a2, a3, bl0 & pm, bl1 & pm);
+    for (int h = 0; h < HP; ++h) {
+      const uint32_t x0 = prmt(va[h][mt >> 1], vb[h][mt >> 1], sel);
+      const uint32_t x1 = prmt(vc[h][mt >> 1], vd[h][mt >> 1], sel);
+      uint32_t a0, a1, a2, a3;
+      e4m3x4_to_f16x2(x0, a0, a1);
+      e4m3x4_to_f16x2(x1, a2, a3);
+      if (tail) {
+        a0 &= vm0;
+        a1 &= vm0;
+        a2 &= vm1;
+        a3 &= vm1;
       }
-      if constexpr (SC) {
-        st.o[mt][0] = fmaf(f0, t4[0], st.o[mt][0]);
-        st.o[mt][1] = fmaf(f1, t4[1], st.o[mt][1]);
-        st.o[mt][2] = fmaf(f0, t4[2], st.o[mt][2]);
-        st.o[mt][3] = fmaf(f1, t4[3], st.o[mt][3]);
-      }
+      const uint32_t pm = HP == 1 || bh == h ? 0xffffffffu : 0u;   // this head's columns
+      mma_f16(st.o[mt], a0, a1, a2, a3, bh0 & pm, bh1 & pm);
+      mma_f16(st.o[mt], a0, a1, a2, a3, bl0 & pm, bl1 & pm);
     }
-  };
-  if (scaled)
-    pv(std::true_type{});
-  else
-    pv(std::false_type{});
+  }
 }
 
 }  // namespace da
