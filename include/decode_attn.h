@@ -115,9 +115,13 @@ typedef struct {
    * finite and > 0; q stays qkv_dtype, which must be DA_BF16 (else DA_ERR_UNSUPPORTED).
    * With groups of 4 query heads over an even number of KV heads, the plan packs pairs of KV
    * heads into one group of the split kernel where the step is large (at least four packed
-   * groups per SM, or a cache capacity of 128 MiB and more); da_plan_info reports it. The codes convert exactly; k_scale enters the logits' FP32 scale
-   * factor and v_scale the output's. NaN codes are not detected (they read as finite
-   * values). kv_fp8 = 0: k_cache and v_cache are qkv_dtype; the scales are not read. */
+   * groups per SM, or a cache capacity of 128 MiB and more); da_plan_info reports it.
+   * The codes convert exactly; k_scale enters the logits' FP32 scale factor and v_scale the
+   * output's. P . V runs on f16, so in the unified modes each split keeps its p = exp(x - phi)
+   * within f16's range by a power-of-two factor per head, which only changes when its largest
+   * logit grows past the range (the outputs and flags are those of the unified softmax).
+   * NaN codes are not detected (they read as finite values). kv_fp8 = 0: k_cache and v_cache
+   * are qkv_dtype; the scales are not read. */
   int kv_fp8;
   float k_scale;
   float v_scale;
