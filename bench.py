@@ -458,6 +458,8 @@ def run_ours(args):
                    "grid_ctas": attn.info.grid_ctas, "stages": attn.info.stages,
                    "split_tokens": [stats.split_tokens_min, stats.split_tokens],
                    "kv_bytes_per_step": kv_bytes,
+                   "inputs_sha256": workloads.input_digest(inp),
+                   "kv_heads_per_group": attn.info.kv_heads_per_group,
                    "timing": "value and ms_per_step from the median step; us_per_step gives median, min, p90 and mean",
                    "l2": f"flushed before every timed step: {FLUSH_BYTES >> 20} MiB written, then {FLUSH_BYTES >> 20} MiB of another buffer read (evicts the dirty lines)",
                    "host_ahead": f"a {HOST_AHEAD_CYCLES}-cycle device spin precedes each timed step, outside its events, so host call overhead is not timed as device time (e2e times it)",

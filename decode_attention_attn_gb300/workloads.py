@@ -199,6 +199,18 @@ def quantize_e4m3(x: torch.Tensor):
     return codes, scale
 
 
+def input_digest(inp: Inputs) -> dict:
+    """The first 16 hex digits of the SHA-256 of each input tensor's stored bytes, so that a
+    measurement names the exact inputs it ran on."""
+    import hashlib
+    out = {}
+    for name in ("q", "k_cache", "v_cache", "block_table", "seq_lens"):
+        t = getattr(inp, name)
+        if t is not None:
+            out[name] = hashlib.sha256(bits(t).tobytes()).hexdigest()[:16]
+    return out
+
+
 def bits(t: torch.Tensor) -> np.ndarray:
     """The tensor's storage as numpy: float32 for fp32, uint16 bit patterns for fp16/bf16,
     the code bytes (uint8) of an FP8 cache."""
